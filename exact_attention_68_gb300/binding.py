@@ -1,0 +1,156 @@
+"""ctypes binding to the C ABI of include/attn.h (argument marshalling only).
+
+Every step of the forward runs in the CUDA library; this module checks
+dtypes/shapes, hands raw device pointers and the current CUDA stream to the C
+functions and turns status codes into exceptions.  torch is used only to own
+device memory and to name the stream.  If the library has not been built the
+first call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = ["AttnError", "load_library", "attn_fwd", "attn_fwd_bounded", "attn_fwd_staged",
+           "device_status", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
+           "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
+ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 3, 4, 5
+
+_i64, _p, _f, _i, _u64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int, ctypes.c_uint64
+_SIGS = {
+    "attn_fwd": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _f, _i, _p]),
+    "attn_fwd_staged": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                             _i64, _i64, _i64, _i64, _f, _i, _p]),
+    "attn_fwd_bounded": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _f, _i, _u64, _p]),
+    "attn_device_status": (_i, [_p]),
+    "attn_status_string": (ctypes.c_char_p, [_i]),
+    "attn_abi_version": (_i, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGS)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _status_string(code)
+        super().__init__(f"{where}: {msg} (status {code})")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load (once) the CUDA library and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library not built: {p} is missing "
+                               "(run `python -m exact_attention_68_gb300.build`)")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _status_string(code: int) -> str:
+    try:
+        return load_library().attn_status_string(int(code)).decode()
+    except Exception:  # library missing: still report the number
+        return "attention library status"
+
+
+def _stream_handle(device: torch.device, stream) -> int:
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, S, D] tensor")
+    if not (q.shape == k.shape == v.shape) or not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must share shape and device")
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+             causal: bool = True, out: torch.Tensor | None = None,
+             lse: torch.Tensor | None = None, stream=None):
+    """Fused attention forward.  Returns (out bf16 [B,H,S,D], lse fp32 [B,H,S])."""
+    return attn_fwd_bounded(q, k, v, scale, causal, out, lse, stream, None)
+
+
+def attn_fwd_bounded(q, k, v, scale=None, causal=True, out=None, lse=None, stream=None,
+                     wait_timeout_ns: int | None = None):
+    """attn_fwd with an explicit bound on every in-kernel wait (None = library default)."""
+    _check_qkv(q, k, v)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if out.dtype != torch.bfloat16 or out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor")
+    lib = load_library()
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            B, H, S, D, float(scale), 1 if causal else 0)
+    with torch.cuda.device(q.device):
+        st = _stream_handle(q.device, stream)
+        if wait_timeout_ns is None:
+            rc = lib.attn_fwd(*args, st)
+        else:
+            rc = lib.attn_fwd_bounded(*args, int(wait_timeout_ns), st)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_staged(q_h, k_h, v_h, out_h, lse_h, q_d, k_d, v_d, out_d, lse_d, scale=None,
+                    causal=True, stream=None):
+    """Forward from host buffers: H2D copies, kernel, D2H copies on one stream."""
+    _check_qkv(q_d, k_d, v_d)
+    B, H, S, D = q_d.shape
+    for name, t in (("q_h", q_h), ("k_h", k_h), ("v_h", v_h), ("out_h", out_h), ("lse_h", lse_h)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q_d.device):
+        rc = lib.attn_fwd_staged(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), out_h.data_ptr(),
+                                 lse_h.data_ptr(), q_d.data_ptr(), k_d.data_ptr(), v_d.data_ptr(),
+                                 out_d.data_ptr(), lse_d.data_ptr(), B, H, S, D, float(scale),
+                                 1 if causal else 0, _stream_handle(q_d.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_staged")
+    return out_h, lse_h
+
+
+def device_status(device=None, stream=None) -> int:
+    """Synchronise the stream, read and clear the device status word (0 = ok)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        return int(lib.attn_device_status(_stream_handle(dev, stream)))

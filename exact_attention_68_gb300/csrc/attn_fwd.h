@@ -1,0 +1,39 @@
+// attn_fwd.h — kernel parameters and launch entry shared by the host API and
+// the kernel translation unit (host-compilable, no device code).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace ea {
+
+// Rows of one Q tile (the tcgen05 M) and of one K/V tile.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+// Q tiles per CTA work unit (two softmax warpgroups ping-pong on the tensor core).
+constexpr int kQTilesPerUnit = 2;
+constexpr int kThreads = 320;  // 8 softmax warps, 1 MMA warp, 1 TMA warp
+
+struct FwdParams {
+  CUtensorMap tm_q;  // q as (D, S, B·H), box 64 x 128 rows, 128-byte swizzle
+  CUtensorMap tm_k;  // k, same box
+  CUtensorMap tm_v;  // v, same box
+  CUtensorMap tm_o;  // out, box 64 x 32 rows (one warp's rows), 128-byte swizzle
+  float* lse;        // [B·H, S]
+  int* status;       // device status word pair (error bits, first wait site)
+  int B, H, S;
+  int n_qt;          // ceil(S / 128)
+  int n_units;       // ceil(n_qt / 2): work units per (b, h)
+  float scale_log2;  // scale · log2(e)
+  uint64_t timeout_ns;
+};
+
+// Dynamic shared memory one CTA of the D-specialised kernel uses.
+size_t fwd_smem_bytes(int D);
+
+// Sets per-kernel attributes (once per device) and launches one forward.
+cudaError_t fwd_launch(const FwdParams& p, int D, bool causal, cudaStream_t stream);
+
+}  // namespace ea

@@ -1,0 +1,484 @@
+// attn_fwd_sm103.cu — fused exact attention forward for GB300 (sm_103a).
+//
+// Computes, per (batch, head), out = softmax(scale·q·kᵀ + causal mask)·v and
+// the row logsumexp, as defined step by step in "Profiling in PyTorch (Part 3):
+// Attention is all you profile", section "Naive attention", evaluated the way
+// that page's "Why flash attention exists" passage describes: K and V are
+// walked in tiles with a running (online) softmax and the output accumulates
+// tile by tile, so the [S, S] scores never leave the chip.  From the
+// FlashAttention-2 blog ("FlashAttention-2 Optimizations"): §2 fully masked
+// K/V tiles are skipped under the causal mask, §3 work is split over the
+// sequence (one CTA per (b, h, 256 query rows)), §1 the softmax does as few
+// non-matmul operations as it can (exp2 with the scale folded in, the 1/l
+// normalisation deferred to the end, and the running max only moved when it
+// grows by more than 2^8, which keeps every exponent ≤ 8 and is exact because
+// the same reference max scales both O and l).
+//
+// GB300 mapping (one CTA per SM: 224 KB of shared memory, all 512 TMEM columns):
+//   warp 9      TMA producer: Q tiles once, then K_j / V_j through two rings of
+//               shared-memory stages guarded by full/empty mbarriers.
+//   warp 8      tcgen05 issuer (one thread): S_t = Q_t·K_jᵀ (A, B from smem) and
+//               O_t += P_t·V_j (A = P from TMEM, B = V from smem, MN-major),
+//               fp32 accumulators in TMEM; completion signalled by
+//               tcgen05.commit on mbarriers.
+//   warps 0-3   softmax/correction/epilogue for Q tile 0 (rows 0-127 of the unit)
+//   warps 4-7   the same for Q tile 1 (rows 128-255).  One thread owns one query
+//               row (its TMEM lane): row max and row sum need no shuffles.
+// While one warpgroup runs the softmax of its tile, the tensor core works on
+// the other tile's MMAs (the two tiles ping-pong).
+//
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+// P_t (bf16, two per 32-bit column) overwrites columns [0,64) of S_t.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn_fwd.h"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace ea {
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+// The running max is only moved when it grows by more than this (log2 units).
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint64_t kDrainLimitNs = 1000000000ull;  // bound on waits while tearing down
+
+template <int D>
+struct Layout {
+  static constexpr int kTileBytes = kBlockM * D * 2;  // one 128-row bf16 tile
+  static constexpr int kChunks = D / 64;              // 64-column (128-byte) swizzle blocks
+  static constexpr int kChunkBytes = kBlockM * 128;   // 16 KB
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQTilesPerUnit * kTileBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  // barriers: q_full[2], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+  //           s_full[2], p_full[2], o_full[2], drain
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort flag (int)
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
+  static_assert(kAlloc <= 232448, "shared memory budget exceeded");
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(2 * 128 + 2 * D <= 512, "TMEM budget exceeded");
+};
+
+struct Bars {
+  uint64_t* q_full;
+  uint64_t* k_full;
+  uint64_t* k_empty;
+  uint64_t* v_full;
+  uint64_t* v_empty;
+  uint64_t* s_full;
+  uint64_t* p_full;
+  uint64_t* o_full;
+  uint64_t* drain;
+};
+
+template <int D>
+__device__ __forceinline__ Bars bars_at(uint8_t* base) {
+  using L = Layout<D>;
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + L::kBarOff);
+  Bars r;
+  r.q_full = b;
+  r.k_full = r.q_full + 2;
+  r.k_empty = r.k_full + L::kKStages;
+  r.v_full = r.k_empty + L::kKStages;
+  r.v_empty = r.v_full + L::kVStages;
+  r.s_full = r.v_empty + L::kVStages;
+  r.p_full = r.s_full + 2;
+  r.o_full = r.p_full + 2;
+  r.drain = r.o_full + 2;
+  return r;
+}
+
+// Wait-site tags recorded in status[1] by the first wait that runs out.
+enum : int {
+  kSiteProducerK = 0x100, kSiteProducerV = 0x200, kSiteMmaQ = 0x300, kSiteMmaK = 0x400,
+  kSiteMmaV = 0x500, kSiteMmaP = 0x600, kSiteSoftS = 0x700, kSiteSoftO = 0x800
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const Bars bar = bars_at<D>(smem);
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: (b·H + h, pair of Q tiles), heaviest units first
+  const int BH = p.B * p.H;
+  const int unit_rev = blockIdx.x / BH;
+  const int bh = blockIdx.x - unit_rev * BH;
+  const int u = p.n_units - 1 - unit_rev;
+  const int qt0 = 2 * u;
+  const int qt1 = 2 * u + 1;
+  const int n0 = CAUSAL ? qt0 + 1 : p.n_qt;
+  const int n1 = (qt1 < p.n_qt) ? (CAUSAL ? qt1 + 1 : p.n_qt) : 0;
+  const int nkv = n0 > n1 ? n0 : n1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.q_full[0], 1);
+    mbar_init(&bar.q_full[1], 1);
+    for (int s = 0; s < L::kKStages; ++s) {
+      mbar_init(&bar.k_full[s], 1);
+      mbar_init(&bar.k_empty[s], 1);
+    }
+    for (int s = 0; s < L::kVStages; ++s) {
+      mbar_init(&bar.v_full[s], 1);
+      mbar_init(&bar.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar.s_full[t], 1);
+      mbar_init(&bar.p_full[t], 128);
+      mbar_init(&bar.o_full[t], 1);
+    }
+    mbar_init(bar.drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_base_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_base_slot;
+
+  WaitCtl ctl;
+  ctl.abort_flag = abort_flag;
+  ctl.status = p.status;
+  ctl.timeout_ns = p.timeout_ns;
+
+  uint8_t* sQ = smem + L::kQOff;
+  uint8_t* sK = smem + L::kKOff;
+  uint8_t* sV = smem + L::kVOff;
+
+  if (warp == 9) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_o);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const int qt[2] = {qt0, qt1};
+      const int nt[2] = {n0, n1};
+      for (int t = 0; t < 2; ++t) {
+        if (nt[t] == 0) continue;
+        mbar_arrive_expect_tx(&bar.q_full[t], L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &p.tm_q, &bar.q_full[t], c * 64,
+                      qt[t] * kBlockM, bh, pol_q);
+      }
+      int k_issued = 0, v_issued = 0;  // K / V tiles whose loads were issued
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        const int ks = j % L::kKStages;
+        ok = wait_bounded(&bar.k_empty[ks], ((j / L::kKStages) & 1) ^ 1, ctl, kSiteProducerK | j);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bar.k_full[ks], L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sK + ks * L::kTileBytes + c * L::kChunkBytes, &p.tm_k, &bar.k_full[ks], c * 64,
+                      j * kBlockN, bh, pol_kv);
+        k_issued = j + 1;
+        const int vs = j % L::kVStages;
+        ok = wait_bounded(&bar.v_empty[vs], ((j / L::kVStages) & 1) ^ 1, ctl, kSiteProducerV | j);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bar.v_full[vs], L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sV + vs * L::kTileBytes + c * L::kChunkBytes, &p.tm_v, &bar.v_full[vs], c * 64,
+                      j * kBlockN, bh, pol_kv);
+        v_issued = j + 1;
+      }
+      if (ok) {
+        // Tail: wait until the tensor core has released every stage, so that
+        // no commit-arrive on a ring barrier can land after this CTA is gone.
+        for (int j = max(nkv - L::kKStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(&bar.k_empty[j % L::kKStages], (j / L::kKStages) & 1, ctl,
+                            kSiteProducerK | 0xff);
+        for (int j = max(nkv - L::kVStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(&bar.v_empty[j % L::kVStages], (j / L::kVStages) & 1, ctl,
+                            kSiteProducerV | 0xff);
+      }
+      if (!ok) {
+        // Abort: let every copy this thread started land before leaving.  The
+        // last load into each stage completes its stage's latest full phase.
+        for (int t = 0; t < 2; ++t)
+          if (nt[t] > 0) wait_drain(&bar.q_full[t], 0, kDrainLimitNs);
+        for (int j = max(k_issued - L::kKStages, 0); j < k_issued; ++j)
+          wait_drain(&bar.k_full[j % L::kKStages], (j / L::kKStages) & 1, kDrainLimitNs);
+        for (int j = max(v_issued - L::kVStages, 0); j < v_issued; ++j)
+          wait_drain(&bar.v_full[j % L::kVStages], (j / L::kVStages) & 1, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 8) {
+    // ======================= tcgen05 issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = instr_desc_bf16(kBlockM, kBlockN, false, false);
+      constexpr uint32_t kIdescO = instr_desc_bf16(kBlockM, D, false, true);
+      const int nt[2] = {n0, n1};
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t k_addr = smem_u32(sK);
+      const uint32_t v_addr = smem_u32(sV);
+
+      auto issue_s = [&](int t, int ks) {
+        const uint32_t a0 = q_addr + t * L::kTileBytes;
+        const uint32_t b0 = k_addr + ks * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem_base + t * 128, smem_desc_sw128(a0 + off, 16, 1024),
+                 smem_desc_sw128(b0 + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int vs, bool accumulate) {
+        const uint32_t b0 = v_addr + vs * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + kk * 8,
+                 smem_desc_sw128(b0 + kk * 2048, L::kChunkBytes, 1024), kIdescO,
+                 (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = true;
+      if (n0 > 0) ok = wait_bounded(&bar.q_full[0], 0, ctl, kSiteMmaQ);
+      if (ok && n1 > 0) ok = wait_bounded(&bar.q_full[1], 0, ctl, kSiteMmaQ | 1);
+      if (ok) ok = wait_bounded(&bar.k_full[0], 0, ctl, kSiteMmaK);
+      if (ok) {
+        tc_fence_after_sync();
+        for (int t = 0; t < 2; ++t) {
+          if (nt[t] == 0) continue;
+          issue_s(t, 0);
+          mma_commit(&bar.s_full[t]);
+        }
+        mma_commit(&bar.k_empty[0]);
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int vs = j % L::kVStages;
+          ok = wait_bounded(&bar.v_full[vs], (j / L::kVStages) & 1, ctl, kSiteMmaV | j);
+          if (!ok) break;
+          const int kn = j + 1;
+          const int ksn = kn % L::kKStages;
+          bool k_next_ready = false;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= nt[t]) continue;
+            ok = wait_bounded(&bar.p_full[t], j & 1, ctl, kSiteMmaP | (t << 7) | j);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_pv(t, vs, j > 0);
+            if (kn < nt[t]) {
+              if (!k_next_ready) {
+                ok = wait_bounded(&bar.k_full[ksn], (kn / L::kKStages) & 1, ctl, kSiteMmaK | kn);
+                if (!ok) break;
+                k_next_ready = true;
+                tc_fence_after_sync();
+              }
+              issue_s(t, ksn);
+              mma_commit(&bar.s_full[t]);
+            } else {
+              mma_commit(&bar.o_full[t]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bar.v_empty[vs]);
+          if (k_next_ready) mma_commit(&bar.k_empty[ksn]);
+        }
+      }
+      // Every MMA this thread issued has completed once `drain` arrives.
+      mma_commit(bar.drain);
+      wait_drain(bar.drain, 0, kDrainLimitNs);
+    }
+  } else {
+    // ======================= softmax / correction / epilogue =======================
+    const int t = warp >> 2;  // Q tile of this warpgroup
+    const int wq = warp & 3;  // TMEM lane quarter of this warp
+    const int row = wq * 32 + lane;
+    const int qt = t == 0 ? qt0 : qt1;
+    const int nt = t == 0 ? n0 : n1;
+    const int grow = qt * kBlockM + row;
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem_base + lane_bits + t * 128;
+    const uint32_t tO = tmem_base + lane_bits + 256 + t * D;
+    const float sl2 = p.scale_log2;
+
+    float m = -INFINITY;  // running max of scale·log2e·s (log2 domain), possibly stale
+    float l = 0.f;        // running sum of p = 2^(t - m) in fp32: gives the logsumexp
+    float lq = 0.f;       // running sum of p rounded to bf16, the weights the tensor
+                          // core multiplies V by: normalises the output, so that
+                          // the rounding of P cancels between numerator and denominator
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = wait_bounded(&bar.s_full[t], j & 1, ctl, kSiteSoftS | (t << 7) | j);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + c * 32, sr[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+
+      // mask: key column > query row (causal diagonal tile) or column >= S (tail)
+      const bool edge = (CAUSAL && j == qt) || ((j + 1) * kBlockN > p.S);
+      if (edge) {
+        int lim = p.S - 1 - j * kBlockN;  // last allowed column inside this tile
+        if (CAUSAL) lim = min(lim, grow - j * kBlockN);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i > lim) sr[c][i] = __float_as_uint(-INFINITY);
+      }
+
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+      const float m_tile = mx * sl2;
+      const float m_new = fmaxf(m, m_tile);
+      float alpha = 1.f;
+      if (j == 0) {
+        m = m_new;
+      } else if (m_new > m + kRescaleThreshold) {
+        alpha = ex2_approx(m - m_new);
+        m = m_new;
+      }
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      float rs = 0.f, rq = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = (h * 64 + 2 * i) >> 5;
+          const int e = (h * 64 + 2 * i) & 31;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, neg_m));
+          const uint32_t u = pack_bf16x2(p0, p1);
+          rs += p0 + p1;
+          rq += __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
+          pk[i] = u;
+        }
+        tmem_st_32x32b_x32(tS + h * 32, pk);
+      }
+      l = l * alpha + rs;
+      lq = lq * alpha + rq;
+      // correction (after P, when the S registers are dead): rescale this row of
+      // O when its reference max moved.  PV_{j-1} has completed: S_j was
+      // committed after it.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_32x32b_x32(tO + c * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&bar.p_full[t]);
+    }
+
+    // ---- epilogue: O / l → bf16 → smem (swizzled) → TMA store; lse
+    if (nt > 0) {
+      if (ok) {
+        ok = wait_bounded(&bar.o_full[t], 0, ctl, kSiteSoftO | t);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after_sync();
+        const float inv_l = lq > 0.f ? 1.f / lq : 0.f;
+        uint8_t* stage = sQ + t * L::kTileBytes;  // Q_t is no longer read by any MMA
+        const uint32_t stage_addr = smem_u32(stage);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int unit = c * 4 + q4;  // 16-byte unit index along the row
+            const int chunk = unit >> 3;
+            const int u16 = unit & 7;
+            const uint32_t addr = stage_addr + chunk * L::kChunkBytes + row * 128 +
+                                  ((u16 ^ (row & 7)) << 4);
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
+                                 __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
+            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_store_3d(&p.tm_o, stage + c * L::kChunkBytes + wq * 32 * 128, c * 64,
+                         qt * kBlockM + wq * 32, bh);
+          tma_store_commit();
+        }
+        if (grow < p.S) {
+          const float lse2 = m + __log2f(l);
+          p.lse[(int64_t)bh * p.S + grow] = lse2 * kLn2;
+        }
+        if (lane == 0) tma_store_wait_all();
+      }
+    }
+    tc_fence_before_sync();
+  }
+
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
+  using L = Layout<D>;
+  auto kern = attn_fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)p.B * p.H * p.n_units;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes(int D) { return D == 64 ? Layout<64>::kAlloc : Layout<128>::kAlloc; }
+
+cudaError_t fwd_launch(const FwdParams& p, int D, bool causal, cudaStream_t stream) {
+  if (D == 64) return causal ? launch_impl<64, true>(p, stream) : launch_impl<64, false>(p, stream);
+  return causal ? launch_impl<128, true>(p, stream) : launch_impl<128, false>(p, stream);
+}
+
+}  // namespace ea

@@ -1,0 +1,133 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) fused exact attention forward.
+ *
+ * The operation (what every entry point below computes) is the one spelled
+ * out step by step in "Profiling in PyTorch (Part 3): Attention is all you
+ * profile", section "Naive attention":
+ *
+ *     scores = q · kᵀ;  scores *= scale;  scores.masked_fill(mask, −inf);
+ *     attn = softmax(scores, dim=-1);  out = attn · v
+ *
+ * with the causal mask of that page's "Math backend" section (ones → tril:
+ * key j > query i is masked) and scale = 1/√head_dim as in its
+ * NaiveCausalAttention module.  It is computed the way the same page's "Why
+ * flash attention exists" passage and the FlashAttention-2 blog
+ * ("FlashAttention (Original)": tiling, reduced HBM reads/writes;
+ * "FlashAttention-2 Optimizations" §2-§3: causal skip, parallelism over the
+ * sequence) describe: K and V are walked in tiles with a running softmax and
+ * the [S, S] score matrix never reaches HBM.  In addition each row's natural
+ * logsumexp  lse[i] = ln Σ_{j unmasked} exp(scale · q_i · k_j)  is written
+ * (the pages do not define it; this is the FlashAttention convention).
+ *
+ * Layout (the native [batch, heads, seq, head_dim] layout the cuDNN backend of
+ * the same page consumes without transposes): q, k, v and out are contiguous
+ * row-major bf16 tensors of shape [B, H, S, D]; lse is contiguous fp32
+ * [B, H, S].  Query and key lengths are equal (S).
+ *
+ * Ownership: the caller owns every buffer.  Apart from one small device
+ * status word per device (allocated on the first call on that device and kept
+ * until process exit) the library allocates nothing, keeps no reference to any
+ * buffer after a call returns, and never synchronises the stream inside
+ * attn_fwd.  Entry points are thread-safe and reentrant.
+ *
+ * Error behaviour: argument errors are reported before anything is launched
+ * and nothing is written.  A failed launch returns ATTN_ERR_CUDA.  Every wait
+ * inside the kernel is bounded; a wait that runs out records ATTN_ERR_TIMEOUT
+ * in the device status word (read with attn_device_status) and the kernel
+ * returns without trapping.
+ */
+#ifndef EXACT_ATTENTION_68_ATTN_H_
+#define EXACT_ATTENTION_68_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, size < 1, overflow, scale not finite and > 0, causal not 0/1, aliasing */
+  ATTN_ERR_UNSUPPORTED = 2,  /* head_dim other than 64 or 128, or no sm_103a device */
+  ATTN_ERR_MISALIGNED = 3,   /* a pointer not 16-byte aligned */
+  ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, tensor-map encode) */
+  ATTN_ERR_TIMEOUT = 5       /* a bounded in-kernel wait ran out (reported by attn_device_status) */
+} attn_status_t;
+
+/*
+ * attn_fwd — fused attention forward on device buffers.
+ *
+ *   q, k, v  device pointers, bf16 [B, H, S, D] contiguous, 16-byte aligned (read only)
+ *   out      device pointer, bf16 [B, H, S, D] contiguous, 16-byte aligned (written)
+ *   lse      device pointer, fp32 [B, H, S] contiguous, 4-byte aligned (written)
+ *   B, H, S  batch, heads, sequence length; each >= 1, B·H < 2^31, S < 2^31
+ *   D        head dimension: 64 or 128
+ *   scale    multiplier of q·kᵀ (normally 1/sqrt(D)); must be finite and > 0
+ *   causal   1: mask key j > query i; 0: no mask
+ *   stream   CUDA stream the work is enqueued on (0 = legacy default stream)
+ *
+ * Asynchronous: returns once the kernel is enqueued.  out/lse must not
+ * overlap q, k, v or each other.
+ */
+ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                       int64_t B, int64_t H, int64_t S, int64_t D, float scale, int causal,
+                       cudaStream_t stream);
+
+/*
+ * attn_fwd_staged — the same forward, fed from and returned to HOST memory.
+ *
+ * q_h, k_h, v_h (bf16 [B,H,S,D]) are copied host→device into the caller's
+ * device buffers q_d, k_d, v_d; attn_fwd runs on them writing out_d, lse_d;
+ * out_d and lse_d are copied back to out_h (bf16 [B,H,S,D]) and lse_h (fp32
+ * [B,H,S]).  All copies are cudaMemcpyAsync on `stream`; pass page-locked
+ * host memory for them to be asynchronous.  Returns after enqueueing; the
+ * host results are valid once the stream is synchronised.  Same argument
+ * rules as attn_fwd for the device side; host pointers must be non-NULL.
+ */
+ATTN_API attn_status_t attn_fwd_staged(const void* q_h, const void* k_h, const void* v_h,
+                              void* out_h, float* lse_h,
+                              void* q_d, void* k_d, void* v_d, void* out_d, float* lse_d,
+                              int64_t B, int64_t H, int64_t S, int64_t D, float scale,
+                              int causal, cudaStream_t stream);
+
+/*
+ * attn_fwd_bounded — attn_fwd with an explicit bound on every in-kernel wait.
+ *
+ * wait_timeout_ns bounds each wait of the kernel on a pipeline barrier
+ * (attn_fwd uses 2 s).  When a wait runs out the kernel records
+ * ATTN_ERR_TIMEOUT in the device status word, every role leaves its loop,
+ * waits (bounded) for its own copies and tensor-core work in flight, frees its
+ * tensor memory and returns.  A bound of 0 makes the first wait that is not
+ * already satisfied run out: this is how the timeout path is tested.
+ */
+ATTN_API attn_status_t attn_fwd_bounded(const void* q, const void* k, const void* v, void* out,
+                               float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                               float scale, int causal, uint64_t wait_timeout_ns,
+                               cudaStream_t stream);
+
+/*
+ * attn_device_status — synchronise `stream`, then read and clear the status
+ * word of the current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel on
+ * this device recorded a timeout since the last read) or ATTN_ERR_CUDA.
+ */
+ATTN_API attn_status_t attn_device_status(cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+ATTN_API const char* attn_status_string(attn_status_t status);
+
+/* ABI version of this library (incremented on any signature change). */
+ATTN_API int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_68_ATTN_H_ */

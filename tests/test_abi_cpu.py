@@ -1,0 +1,97 @@
+"""CPU checks of the C-ABI library: it loads, exports every declared symbol,
+and rejects bad arguments before touching the GPU (no compute call here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_68_gb300 import binding
+from exact_attention_68_gb300.build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build_library()
+    return binding.load_library(path)
+
+
+def _declared():
+    with open(HEADER) as f:
+        src = f.read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", src)
+
+
+def test_header_declares_the_bound_symbols():
+    names = _declared()
+    assert sorted(names) == sorted(binding.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert lib.attn_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(0) == b"ok"
+
+
+# Fake, never dereferenced device addresses: validation runs before any CUDA call.
+A = 0x7F0000000000
+T = 1 << 30  # spacing large enough for the shapes used below
+
+
+def _call(lib, q=A, k=A + T, v=A + 2 * T, out=A + 3 * T, lse=A + 4 * T,
+          B=1, H=2, S=128, D=64, scale=0.125, causal=1):
+    return lib.attn_fwd(q, k, v, out, lse, B, H, S, D, scale, causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(k=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(v=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(out=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(H=-1), binding.ATTN_ERR_INVALID_ARG),
+    (dict(S=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(D=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-0.5), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), binding.ATTN_ERR_INVALID_ARG),
+    (dict(q=A + 8), binding.ATTN_ERR_MISALIGNED),
+    (dict(out=A + 3 * T + 2), binding.ATTN_ERR_MISALIGNED),
+    (dict(lse=A + 4 * T + 1), binding.ATTN_ERR_MISALIGNED),
+    (dict(out=A), binding.ATTN_ERR_INVALID_ARG),                # out aliases q
+    (dict(lse=A + 3 * T + 64), binding.ATTN_ERR_INVALID_ARG),   # lse inside out
+    (dict(B=1 << 31), binding.ATTN_ERR_INVALID_ARG),
+    (dict(B=1 << 20, H=1 << 20), binding.ATTN_ERR_INVALID_ARG),
+    (dict(B=1 << 16, H=1 << 14, S=1 << 20), binding.ATTN_ERR_INVALID_ARG),
+])
+def test_invalid_arguments_are_rejected_before_launch(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+def test_bounded_and_staged_validate_too(lib):
+    assert lib.attn_fwd_bounded(0, A, A, A + 3 * T, A + 4 * T, 1, 1, 128, 64, 0.125, 1, 0, None) \
+        == binding.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_staged(0, A, A, A, A, A, A + T, A + 2 * T, A + 3 * T, A + 4 * T,
+                               1, 1, 128, 64, 0.125, 1, None) == binding.ATTN_ERR_INVALID_ARG
+    # the same device buffer for q and k cannot hold two different host inputs
+    assert lib.attn_fwd_staged(A, A, A, A, A, A, A, A + 2 * T, A + 3 * T, A + 4 * T,
+                               1, 1, 128, 64, 0.125, 1, None) == binding.ATTN_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load_library(str(tmp_path / "missing.so"))

@@ -1,0 +1,144 @@
+"""GPU parity: the CUDA forward against the fp64 oracle on the same seeded inputs.
+
+Every call goes through the C ABI (the ctypes binding).  Bar (against the
+unrounded oracle): max |out err| <= 2e-2, mean |out err| <= 2e-3,
+max |lse err| <= 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_68_gb300 import binding
+from exact_attention_68_gb300.workloads import WORKLOADS, check_rows, default_scale, make_qkv
+from gpu_helpers import compare, run_gpu, to_f64
+from oracle import attention_fwd, attention_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_rows(q, k, v, scale, causal, idx):
+    return attention_rows(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, causal, idx)
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_workload_parity(cuda_device, name):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w, seed=0)
+    scale = default_scale(w.D)
+    out, lse = run_gpu(q, k, v, scale, w.causal)
+    idx = check_rows(w)
+    ro, rl = _oracle_rows(q, k, v, scale, w.causal, idx)
+    og = to_f64(out)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    lg = to_f64(lse)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    s = compare(og, lg, ro, rl, name)
+    print(name, s)
+
+
+EDGE_SHAPES = [
+    (1, 1, 1, 64), (1, 1, 1, 128), (1, 1, 7, 64), (1, 1, 7, 128), (2, 3, 129, 64),
+    (1, 2, 200, 128), (1, 1, 256, 128), (1, 1, 384, 64), (3, 1, 1000, 128), (1, 2, 640, 64),
+    (2, 1, 513, 128),
+]
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_edge_shapes_full_oracle(cuda_device, shape, causal):
+    q, k, v = make_qkv(shape, seed=11)
+    scale = default_scale(shape[3])
+    out, lse = run_gpu(q, k, v, scale, causal)
+    ro, rl = attention_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, causal)
+    compare(to_f64(out), to_f64(lse), ro, rl, f"{shape} causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [0.03, 0.5])
+@pytest.mark.parametrize("D", [64, 128])
+def test_other_scales(cuda_device, scale, D):
+    q, k, v = make_qkv((2, 2, 300, D), seed=5, qk_std=2.0)
+    for causal in (True, False):
+        out, lse = run_gpu(q, k, v, scale, causal)
+        ro, rl = attention_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, causal)
+        compare(to_f64(out), to_f64(lse), ro, rl, f"scale={scale} D={D} causal={causal}")
+
+
+def test_peaked_softmax_many_rescales(cuda_device):
+    """Large logits whose running max keeps climbing along the keys."""
+    q, k, v = make_qkv((1, 4, 1024, 128), seed=6, qk_std=4.0)
+    # make later keys larger so the running max moves at many tiles
+    ramp = torch.linspace(0.5, 2.0, 1024).view(1, 1, 1024, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    scale = default_scale(128)
+    for causal in (True, False):
+        out, lse = run_gpu(q, k, v, scale, causal)
+        ro, rl = attention_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, causal)
+        compare(to_f64(out), to_f64(lse), ro, rl, f"peaked causal={causal}")
+
+
+def test_constant_v_closed_form(cuda_device):
+    """Every V row equal to c gives out = c (rounded to bf16) for every row."""
+    q, k, _ = make_qkv((1, 2, 777, 128), seed=8)
+    c = torch.linspace(-3, 3, 128).to(torch.bfloat16)
+    v = c.view(1, 1, 1, 128).expand(1, 2, 777, 128).contiguous()
+    for causal in (True, False):
+        out, _ = run_gpu(q, k, v, default_scale(128), causal)
+        err = (out.double() - c.double()).abs().max().item()
+        assert err <= 2e-2
+
+
+def test_first_causal_row_is_v0(cuda_device):
+    q, k, v = make_qkv((2, 3, 512, 64), seed=9)
+    out, lse = run_gpu(q, k, v, default_scale(64), True)
+    np.testing.assert_array_equal(out[:, :, 0].float().numpy(), v[:, :, 0].float().numpy())
+    ref = (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1) * default_scale(64)
+    assert (lse[:, :, 0].double() - ref).abs().max().item() <= 1e-3
+
+
+def test_causal_rows_ignore_later_keys_bitwise(cuda_device):
+    """Changing K/V rows after i leaves rows <= i bit-identical (c3 shape)."""
+    w = WORKLOADS["c3"]
+    q, k, v = make_qkv(w, seed=0)
+    scale = default_scale(w.D)
+    out1, lse1 = run_gpu(q, k, v, scale, True)
+    i0 = 1000  # inside a Q tile, so the diagonal tile is partly perturbed
+    k2, v2 = k.clone(), v.clone()
+    g = torch.Generator().manual_seed(99)
+    k2[:, :, i0 + 1:] = torch.randn(k2[:, :, i0 + 1:].shape, generator=g).to(torch.bfloat16)
+    v2[:, :, i0 + 1:] = torch.randn(v2[:, :, i0 + 1:].shape, generator=g).to(torch.bfloat16)
+    out2, lse2 = run_gpu(q, k2, v2, scale, True)
+    assert torch.equal(out1[:, :, :i0 + 1], out2[:, :, :i0 + 1])
+    assert torch.equal(lse1[:, :, :i0 + 1], lse2[:, :, :i0 + 1])
+    assert not torch.equal(out1[:, :, i0 + 1:], out2[:, :, i0 + 1:])
+
+
+def test_bitwise_deterministic(cuda_device):
+    w = WORKLOADS["c2"]
+    q, k, v = make_qkv(w, seed=0)
+    a = run_gpu(q, k, v, default_scale(w.D), True)
+    b = run_gpu(q, k, v, default_scale(w.D), True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_staged_host_entry_point_matches(cuda_device):
+    q, k, v = make_qkv((1, 4, 1024, 128), seed=12)
+    scale = default_scale(128)
+    ref_out, ref_lse = run_gpu(q, k, v, scale, True)
+    qh, kh, vh = (x.pin_memory() for x in (q, k, v))
+    out_h = torch.empty_like(q).pin_memory()
+    lse_h = torch.empty(ref_lse.shape, dtype=torch.float32).pin_memory()
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (torch.empty_like(x, device=dev) for x in (q, k, v))
+    od = torch.empty_like(qd)
+    ld = torch.empty(ref_lse.shape, dtype=torch.float32, device=dev)
+    binding.attn_fwd_staged(qh, kh, vh, out_h, lse_h, qd, kd, vd, od, ld, scale=scale, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, ref_out) and torch.equal(lse_h, ref_lse)
+
+
+def test_binding_rejects_wrong_dtype_and_layout(cuda_device):
+    q, k, v = (x.to("cuda:0") for x in make_qkv((1, 1, 128, 64)))
+    with pytest.raises(TypeError):
+        binding.attn_fwd(q.float(), k, v)
+    with pytest.raises(ValueError):
+        binding.attn_fwd(q.transpose(1, 2), k, v)
+    with pytest.raises(binding.AttnError):
+        binding.attn_fwd(q, k, v, scale=-1.0)
