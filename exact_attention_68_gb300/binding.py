@@ -18,7 +18,7 @@ import torch
 from .build import LIB_PATH
 
 __all__ = ["AttnError", "load_library", "attn_fwd", "attn_fwd_bounded", "attn_fwd_staged",
-           "device_status", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
+           "attn_fwd_noalloc", "device_status", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
@@ -30,6 +30,7 @@ _SIGS = {
     "attn_fwd_staged": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                              _i64, _i64, _i64, _i64, _f, _i, _p]),
     "attn_fwd_bounded": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _f, _i, _u64, _p]),
+    "attn_fwd_noalloc": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _f, _i, _i, _p]),
     "attn_device_status": (_i, [_p]),
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_abi_version": (_i, []),
@@ -146,6 +147,31 @@ def attn_fwd_staged(q_h, k_h, v_h, out_h, lse_h, q_d, k_d, v_d, out_d, lse_d, sc
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_staged")
     return out_h, lse_h
+
+
+def attn_fwd_noalloc(q, k, v, out, lse, scale=None, causal=True, check_status=True, stream=None):
+    """Forward through attn_fwd_noalloc: the library allocates no device memory.
+
+    ``out`` and ``lse`` are required (the caller owns all memory).  With
+    ``check_status`` the call synchronises the stream and raises AttnError if
+    the kernel recorded an in-kernel wait that ran out.
+    """
+    _check_qkv(q, k, v)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out.dtype != torch.bfloat16 or out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, H, S, D, float(scale), 1 if causal else 0,
+                                  1 if check_status else 0, _stream_handle(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_noalloc")
+    return out, lse
 
 
 def device_status(device=None, stream=None) -> int:

@@ -35,7 +35,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return [os.path.join(CSRC, f) for f in ("attn_api.cu", "attn_fwd_sm103.cu")]
+    return [os.path.join(CSRC, f) for f in ("attn_api.cu", "attn_fwd_sm103.cu", "attn_noalloc.cu")]
 
 
 def _deps():

@@ -11,6 +11,7 @@
 
 #include "../../include/attn.h"
 #include "attn_fwd.h"
+#include "attn_host.h"
 #include "tmap.h"
 
 namespace {
@@ -98,32 +99,49 @@ attn_status_t launch(const void* q, const void* k, const void* v, void* out, flo
   DeviceState* st = nullptr;
   attn_status_t s = device_state(&dev, &st);
   if (s != ATTN_OK) return s;
+  return ea::launch_with_status(q, k, v, out, lse, B, H, S, D, scale, causal, timeout_ns,
+                                st->status, stream);
+}
 
-  ea::FwdParams p;
+}  // namespace
+
+namespace ea {
+
+attn_status_t validate_args(const void* q, const void* k, const void* v, const void* out,
+                            const void* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                            float scale, int causal) {
+  return validate(q, k, v, out, lse, B, H, S, D, scale, causal);
+}
+
+attn_status_t launch_with_status(const void* q, const void* k, const void* v, void* out,
+                                 float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                                 float scale, int causal, uint64_t timeout_ns, int* status,
+                                 cudaStream_t stream) {
+  FwdParams p;
   std::memset(&p, 0, sizeof(p));
   const int64_t BH = B * H;
-  if (!ea::encode_bhsd_bf16(&p.tm_q, q, BH, S, D, ea::kBlockM) ||
-      !ea::encode_bhsd_bf16(&p.tm_k, k, BH, S, D, ea::kBlockN) ||
-      !ea::encode_bhsd_bf16(&p.tm_v, v, BH, S, D, ea::kBlockN) ||
-      !ea::encode_bhsd_bf16(&p.tm_o, out, BH, S, D, 32))
+  if (!encode_bhsd_bf16(&p.tm_q, q, BH, S, D, kBlockM) ||
+      !encode_bhsd_bf16(&p.tm_k, k, BH, S, D, kBlockN) ||
+      !encode_bhsd_bf16(&p.tm_v, v, BH, S, D, kBlockN) ||
+      !encode_bhsd_bf16(&p.tm_o, out, BH, S, D, 32))
     return ATTN_ERR_CUDA;
   p.lse = lse;
-  p.status = st->status;
+  p.status = status;
   p.B = static_cast<int>(B);
   p.H = static_cast<int>(H);
   p.S = static_cast<int>(S);
-  p.n_qt = static_cast<int>((S + ea::kBlockM - 1) / ea::kBlockM);
-  p.n_units = (p.n_qt + ea::kQTilesPerUnit - 1) / ea::kQTilesPerUnit;
+  p.n_qt = static_cast<int>((S + kBlockM - 1) / kBlockM);
+  p.n_units = (p.n_qt + kQTilesPerUnit - 1) / kQTilesPerUnit;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout_ns;
-  if (ea::fwd_launch(p, static_cast<int>(D), causal != 0, stream) != cudaSuccess) {
+  if (fwd_launch(p, static_cast<int>(D), causal != 0, stream) != cudaSuccess) {
     (void)cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
   return ATTN_OK;
 }
 
-}  // namespace
+}  // namespace ea
 
 extern "C" {
 

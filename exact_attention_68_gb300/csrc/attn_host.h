@@ -1,0 +1,25 @@
+// attn_host.h — host helpers shared by the C-ABI translation units: argument
+// validation and the tensor-map + launch step with a caller-chosen status
+// word pair.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "../../include/attn.h"
+
+namespace ea {
+
+// Argument checks of attn_fwd; touches no CUDA API.
+attn_status_t validate_args(const void* q, const void* k, const void* v, const void* out,
+                            const void* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                            float scale, int causal);
+
+// Encodes the tensor maps and launches the forward with `status` (device
+// int[2]: error bits, first wait site that ran out) as its status words.
+attn_status_t launch_with_status(const void* q, const void* k, const void* v, void* out,
+                                 float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                                 float scale, int causal, uint64_t timeout_ns, int* status,
+                                 cudaStream_t stream);
+
+}  // namespace ea

@@ -120,6 +120,39 @@ ATTN_API attn_status_t attn_fwd_bounded(const void* q, const void* k, const void
  */
 ATTN_API attn_status_t attn_device_status(cudaStream_t stream);
 
+/*
+ * attn_fwd_noalloc — attn_fwd for callers that must not allocate device memory.
+ *
+ * The pages have no counterpart to this entry point.  It exists for programs
+ * whose device memory belongs to their own allocator (memory reserved up front
+ * and handed out in slices), code held to a fixed device-memory budget, and
+ * latency-critical paths that may not pay for cudaMalloc, which can
+ * synchronise the whole device.  attn_fwd allocates its device status words
+ * with cudaMalloc on its first call on each device; this entry point keeps
+ * them in a static device array of ATTN_NOALLOC_SCRATCH_BYTES instead, held
+ * by every GPU that loads the library until the process exits, and calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, layout, ownership and argument errors are those of attn_fwd.
+ * check_status: 0 = return once enqueued; 1 = also synchronise `stream` and
+ * return ATTN_ERR_TIMEOUT if this call's kernel recorded a wait that ran out.
+ * The scratch this kernel needs (two status words, 8 bytes) does not grow with
+ * B, H, S or D; a need above ATTN_NOALLOC_SCRATCH_BYTES is rejected with
+ * ATTN_ERR_INVALID_ARG before anything is enqueued.
+ *
+ * The first call on a device sets that device up (looks up the device address
+ * of the array with the device current); make that first call before any
+ * stream capture.  Every call on a device shares the one array and clears it
+ * (cudaMemsetAsync on `stream`) before its kernel starts: calls whose work
+ * overlaps on the GPU (different streams, or another host thread) race on it,
+ * and a status read may then belong to another call.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES 256
+ATTN_API attn_status_t attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
+                                        float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                                        float scale, int causal, int check_status,
+                                        cudaStream_t stream);
+
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status_t status);
 

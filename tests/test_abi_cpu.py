@@ -95,3 +95,14 @@ def test_bounded_and_staged_validate_too(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         binding.load_library(str(tmp_path / "missing.so"))
+
+
+def test_noalloc_validates_before_touching_the_gpu(lib):
+    args = [A, A + T, A + 2 * T, A + 3 * T, A + 4 * T, 1, 2, 128, 64, 0.125, 1]
+    assert lib.attn_fwd_noalloc(*args, 2, None) == binding.ATTN_ERR_INVALID_ARG  # check_status
+    bad = list(args)
+    bad[0] = 0
+    assert lib.attn_fwd_noalloc(*bad, 1, None) == binding.ATTN_ERR_INVALID_ARG
+    bad = list(args)
+    bad[8] = 80
+    assert lib.attn_fwd_noalloc(*bad, 1, None) == binding.ATTN_ERR_UNSUPPORTED
