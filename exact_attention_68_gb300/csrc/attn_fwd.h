@@ -14,7 +14,13 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 // Q tiles per CTA work unit (two softmax warpgroups ping-pong on the tensor core).
 constexpr int kQTilesPerUnit = 2;
-constexpr int kThreads = 320;  // 8 softmax warps, 1 MMA warp, 1 TMA warp
+// Warps 0-7: two softmax warpgroups; warps 8-11: control warpgroup (warp 8 MMA
+// issuer, warp 9 TMA producer, warps 10-11 idle).
+constexpr int kThreads = 384;
+// Register split set with setmaxnreg; launch budget 384 x 168 = 64512 >=
+// 256 x 200 + 128 x 72 = 60416.
+constexpr int kSoftmaxRegs = 200;
+constexpr int kControlRegs = 72;
 
 struct FwdParams {
   CUtensorMap tm_q;  // q as (D, S, B·H), box 64 x 128 rows, 128-byte swizzle

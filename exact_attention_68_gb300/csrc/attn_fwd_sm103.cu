@@ -14,18 +14,20 @@
 // grows by more than 2^8, which keeps every exponent ≤ 8 and is exact because
 // the same reference max scales both O and l).
 //
-// GB300 mapping (one CTA per SM: 224 KB of shared memory, all 512 TMEM columns):
-//   warp 9      TMA producer: Q tiles once, then K_j / V_j through two rings of
-//               shared-memory stages guarded by full/empty mbarriers.
+// GB300 mapping (one CTA per SM: 225 KB of shared memory, all 512 TMEM columns):
+//   warps 0-3   softmax/correction/epilogue for Q tile 0 (rows 0-127 of the unit)
+//   warps 4-7   the same for Q tile 1 (rows 128-255).  One thread owns one query
+//               row (its TMEM lane): row max and row sums need no shuffles.
 //   warp 8      tcgen05 issuer (one thread): S_t = Q_t·K_jᵀ (A, B from smem) and
 //               O_t += P_t·V_j (A = P from TMEM, B = V from smem, MN-major),
 //               fp32 accumulators in TMEM; completion signalled by
-//               tcgen05.commit on mbarriers.
-//   warps 0-3   softmax/correction/epilogue for Q tile 0 (rows 0-127 of the unit)
-//   warps 4-7   the same for Q tile 1 (rows 128-255).  One thread owns one query
-//               row (its TMEM lane): row max and row sum need no shuffles.
-// While one warpgroup runs the softmax of its tile, the tensor core works on
-// the other tile's MMAs (the two tiles ping-pong).
+//               tcgen05.commit on mbarriers.  Also owns the TMEM allocation.
+//   warp 9      TMA producer: Q tiles once, then K_j / V_j through two rings of
+//               shared-memory stages guarded by full/empty mbarriers.
+//   warps 10-11 idle (they complete the control warpgroup for setmaxnreg).
+// The softmax warpgroups run with 200 registers (a whole row of S stays in
+// registers), the control warpgroup with 72.  While one softmax warpgroup
+// works, the tensor core runs the other tile's MMAs (the two tiles ping-pong).
 //
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
 // P_t (bf16, two per 32-bit column) overwrites columns [0,64) of S_t.
@@ -56,9 +58,17 @@ struct Layout {
   static constexpr int kKOff = kQOff + kQTilesPerUnit * kTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
-  // barriers: q_full[2], k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
-  //           s_full[2], p_full[2], o_full[2], drain
-  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1;
+  // barrier indices (8 bytes each from kBarOff)
+  static constexpr int kQFull = 0;                     // [2]  Q_t landed
+  static constexpr int kKFull = kQFull + 2;            // [KS] K stage landed
+  static constexpr int kKEmpty = kKFull + kKStages;    // [KS] K stage released by the MMAs
+  static constexpr int kVFull = kKEmpty + kKStages;    // [VS]
+  static constexpr int kVEmpty = kVFull + kVStages;    // [VS]
+  static constexpr int kSFull = kVEmpty + kVStages;    // [2]  S_t computed
+  static constexpr int kPFull = kSFull + 2;            // [2]  P_t stored (128 arrivals)
+  static constexpr int kOFull = kPFull + 2;            // [2]  O_t final
+  static constexpr int kDrain = kOFull + 2;            // MMA drain
+  static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base (u32), abort flag (int)
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
@@ -66,35 +76,6 @@ struct Layout {
   static constexpr uint32_t kTmemCols = 512;
   static_assert(2 * 128 + 2 * D <= 512, "TMEM budget exceeded");
 };
-
-struct Bars {
-  uint64_t* q_full;
-  uint64_t* k_full;
-  uint64_t* k_empty;
-  uint64_t* v_full;
-  uint64_t* v_empty;
-  uint64_t* s_full;
-  uint64_t* p_full;
-  uint64_t* o_full;
-  uint64_t* drain;
-};
-
-template <int D>
-__device__ __forceinline__ Bars bars_at(uint8_t* base) {
-  using L = Layout<D>;
-  uint64_t* b = reinterpret_cast<uint64_t*>(base + L::kBarOff);
-  Bars r;
-  r.q_full = b;
-  r.k_full = r.q_full + 2;
-  r.k_empty = r.k_full + L::kKStages;
-  r.v_full = r.k_empty + L::kKStages;
-  r.v_empty = r.v_full + L::kVStages;
-  r.s_full = r.v_empty + L::kVStages;
-  r.p_full = r.s_full + 2;
-  r.o_full = r.p_full + 2;
-  r.drain = r.o_full + 2;
-  return r;
-}
 
 // Wait-site tags recorded in status[1] by the first wait that runs out.
 enum : int {
@@ -106,11 +87,11 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const Bars bar = bars_at<D>(smem);
-  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  // 1024-byte aligned base of the shared window (128-byte swizzle atoms)
+  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  auto bar = [sb](int idx) -> uint32_t { return sb + L::kBarOff + 8u * idx; };
+  const uint32_t tmem_slot = sb + L::kMiscOff;
+  const uint32_t abort_addr = sb + L::kMiscOff + 4;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -127,181 +108,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int nkv = n0 > n1 ? n0 : n1;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar.q_full[0], 1);
-    mbar_init(&bar.q_full[1], 1);
-    for (int s = 0; s < L::kKStages; ++s) {
-      mbar_init(&bar.k_full[s], 1);
-      mbar_init(&bar.k_empty[s], 1);
-    }
-    for (int s = 0; s < L::kVStages; ++s) {
-      mbar_init(&bar.v_full[s], 1);
-      mbar_init(&bar.v_empty[s], 1);
-    }
+#pragma unroll
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bar.s_full[t], 1);
-      mbar_init(&bar.p_full[t], 128);
-      mbar_init(&bar.o_full[t], 1);
+      mbar_init(bar(L::kQFull + t), 1);
+      mbar_init(bar(L::kSFull + t), 1);
+      mbar_init(bar(L::kPFull + t), 128);
+      mbar_init(bar(L::kOFull + t), 1);
     }
-    mbar_init(bar.drain, 1);
-    *abort_flag = 0;
+#pragma unroll
+    for (int s = 0; s < L::kKStages; ++s) {
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+    }
+#pragma unroll
+    for (int s = 0; s < L::kVStages; ++s) {
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+    }
+    mbar_init(bar(L::kDrain), 1);
+    st_volatile_shared(abort_addr, 0);
     fence_barrier_init();
   }
   if (warp == 8) {
-    tmem_alloc(tmem_base_slot, L::kTmemCols);
+    tmem_alloc(tmem_slot, L::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem_base = *tmem_base_slot;
+  const uint32_t tmem_base = static_cast<uint32_t>(ld_volatile_shared(tmem_slot));
 
-  WaitCtl ctl;
-  ctl.abort_flag = abort_flag;
-  ctl.status = p.status;
-  ctl.timeout_ns = p.timeout_ns;
-
-  uint8_t* sQ = smem + L::kQOff;
-  uint8_t* sK = smem + L::kKOff;
-  uint8_t* sV = smem + L::kVOff;
-
-  if (warp == 9) {
-    // ======================= TMA producer =======================
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      tma_prefetch_desc(&p.tm_o);
-      const uint64_t pol_q = l2_policy_evict_first();
-      const uint64_t pol_kv = l2_policy_evict_last();
-      const int qt[2] = {qt0, qt1};
-      const int nt[2] = {n0, n1};
-      for (int t = 0; t < 2; ++t) {
-        if (nt[t] == 0) continue;
-        mbar_arrive_expect_tx(&bar.q_full[t], L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &p.tm_q, &bar.q_full[t], c * 64,
-                      qt[t] * kBlockM, bh, pol_q);
-      }
-      int k_issued = 0, v_issued = 0;  // K / V tiles whose loads were issued
-      bool ok = true;
-      for (int j = 0; j < nkv; ++j) {
-        const int ks = j % L::kKStages;
-        ok = wait_bounded(&bar.k_empty[ks], ((j / L::kKStages) & 1) ^ 1, ctl, kSiteProducerK | j);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bar.k_full[ks], L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sK + ks * L::kTileBytes + c * L::kChunkBytes, &p.tm_k, &bar.k_full[ks], c * 64,
-                      j * kBlockN, bh, pol_kv);
-        k_issued = j + 1;
-        const int vs = j % L::kVStages;
-        ok = wait_bounded(&bar.v_empty[vs], ((j / L::kVStages) & 1) ^ 1, ctl, kSiteProducerV | j);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bar.v_full[vs], L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sV + vs * L::kTileBytes + c * L::kChunkBytes, &p.tm_v, &bar.v_full[vs], c * 64,
-                      j * kBlockN, bh, pol_kv);
-        v_issued = j + 1;
-      }
-      if (ok) {
-        // Tail: wait until the tensor core has released every stage, so that
-        // no commit-arrive on a ring barrier can land after this CTA is gone.
-        for (int j = max(nkv - L::kKStages, 0); j < nkv && ok; ++j)
-          ok = wait_bounded(&bar.k_empty[j % L::kKStages], (j / L::kKStages) & 1, ctl,
-                            kSiteProducerK | 0xff);
-        for (int j = max(nkv - L::kVStages, 0); j < nkv && ok; ++j)
-          ok = wait_bounded(&bar.v_empty[j % L::kVStages], (j / L::kVStages) & 1, ctl,
-                            kSiteProducerV | 0xff);
-      }
-      if (!ok) {
-        // Abort: let every copy this thread started land before leaving.  The
-        // last load into each stage completes its stage's latest full phase.
-        for (int t = 0; t < 2; ++t)
-          if (nt[t] > 0) wait_drain(&bar.q_full[t], 0, kDrainLimitNs);
-        for (int j = max(k_issued - L::kKStages, 0); j < k_issued; ++j)
-          wait_drain(&bar.k_full[j % L::kKStages], (j / L::kKStages) & 1, kDrainLimitNs);
-        for (int j = max(v_issued - L::kVStages, 0); j < v_issued; ++j)
-          wait_drain(&bar.v_full[j % L::kVStages], (j / L::kVStages) & 1, kDrainLimitNs);
-      }
-    }
-  } else if (warp == 8) {
-    // ======================= tcgen05 issuer =======================
-    if (lane == 0) {
-      constexpr uint32_t kIdescS = instr_desc_bf16(kBlockM, kBlockN, false, false);
-      constexpr uint32_t kIdescO = instr_desc_bf16(kBlockM, D, false, true);
-      const int nt[2] = {n0, n1};
-      const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t k_addr = smem_u32(sK);
-      const uint32_t v_addr = smem_u32(sV);
-
-      auto issue_s = [&](int t, int ks) {
-        const uint32_t a0 = q_addr + t * L::kTileBytes;
-        const uint32_t b0 = k_addr + ks * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem_base + t * 128, smem_desc_sw128(a0 + off, 16, 1024),
-                 smem_desc_sw128(b0 + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int t, int vs, bool accumulate) {
-        const uint32_t b0 = v_addr + vs * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + kk * 8,
-                 smem_desc_sw128(b0 + kk * 2048, L::kChunkBytes, 1024), kIdescO,
-                 (accumulate || kk > 0) ? 1u : 0u);
-        }
-      };
-
-      bool ok = true;
-      if (n0 > 0) ok = wait_bounded(&bar.q_full[0], 0, ctl, kSiteMmaQ);
-      if (ok && n1 > 0) ok = wait_bounded(&bar.q_full[1], 0, ctl, kSiteMmaQ | 1);
-      if (ok) ok = wait_bounded(&bar.k_full[0], 0, ctl, kSiteMmaK);
-      if (ok) {
-        tc_fence_after_sync();
-        for (int t = 0; t < 2; ++t) {
-          if (nt[t] == 0) continue;
-          issue_s(t, 0);
-          mma_commit(&bar.s_full[t]);
-        }
-        mma_commit(&bar.k_empty[0]);
-        for (int j = 0; j < nkv && ok; ++j) {
-          const int vs = j % L::kVStages;
-          ok = wait_bounded(&bar.v_full[vs], (j / L::kVStages) & 1, ctl, kSiteMmaV | j);
-          if (!ok) break;
-          const int kn = j + 1;
-          const int ksn = kn % L::kKStages;
-          bool k_next_ready = false;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j >= nt[t]) continue;
-            ok = wait_bounded(&bar.p_full[t], j & 1, ctl, kSiteMmaP | (t << 7) | j);
-            if (!ok) break;
-            tc_fence_after_sync();
-            issue_pv(t, vs, j > 0);
-            if (kn < nt[t]) {
-              if (!k_next_ready) {
-                ok = wait_bounded(&bar.k_full[ksn], (kn / L::kKStages) & 1, ctl, kSiteMmaK | kn);
-                if (!ok) break;
-                k_next_ready = true;
-                tc_fence_after_sync();
-              }
-              issue_s(t, ksn);
-              mma_commit(&bar.s_full[t]);
-            } else {
-              mma_commit(&bar.o_full[t]);
-            }
-          }
-          if (!ok) break;
-          mma_commit(&bar.v_empty[vs]);
-          if (k_next_ready) mma_commit(&bar.k_empty[ksn]);
-        }
-      }
-      // Every MMA this thread issued has completed once `drain` arrives.
-      mma_commit(bar.drain);
-      wait_drain(bar.drain, 0, kDrainLimitNs);
-    }
-  } else {
+  if (warp < 8) {
+    warpgroup_reg_acquire<kSoftmaxRegs>();
     // ======================= softmax / correction / epilogue =======================
+    const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
     const int t = warp >> 2;  // Q tile of this warpgroup
     const int wq = warp & 3;  // TMEM lane quarter of this warp
     const int row = wq * 32 + lane;
@@ -320,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                           // the rounding of P cancels between numerator and denominator
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = wait_bounded(&bar.s_full[t], j & 1, ctl, kSiteSoftS | (t << 7) | j);
+      ok = wait_bounded(bar(L::kSFull + t), j & 1, ctl, kSiteSoftS | (t << 7) | j);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
@@ -344,13 +184,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (c * 32 + i > lim) sr[c][i] = __float_as_uint(-INFINITY);
       }
 
-      float mx = -INFINITY;
+      // row max: 16 independent three-input chains of 8 scores, then a tree
+      float cm[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
-      const float m_tile = mx * sl2;
-      const float m_new = fmaxf(m, m_tile);
+      for (int g = 0; g < 16; ++g) {
+        const uint32_t* e = &sr[g >> 2][(g & 3) * 8];
+        float a = max3f(__uint_as_float(e[0]), __uint_as_float(e[1]), __uint_as_float(e[2]));
+        a = max3f(a, __uint_as_float(e[3]), __uint_as_float(e[4]));
+        a = max3f(a, __uint_as_float(e[5]), __uint_as_float(e[6]));
+        cm[g] = fmaxf(a, __uint_as_float(e[7]));
+      }
+      const float mx = fmaxf(max3f(max3f(cm[0], cm[1], cm[2]), max3f(cm[3], cm[4], cm[5]),
+                                   max3f(cm[6], cm[7], cm[8])),
+                             max3f(max3f(cm[9], cm[10], cm[11]), max3f(cm[12], cm[13], cm[14]),
+                                   cm[15]));
+      const float m_new = fmaxf(m, mx * sl2);
       float alpha = 1.f;
       if (j == 0) {
         m = m_new;
@@ -359,7 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         m = m_new;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float rs = 0.f, rq = 0.f;
+      // p = 2^(s·scale·log2e − m), two scores per packed FMA; four independent
+      // packed accumulators for each of the two row sums
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 nm2 = make_float2(neg_m, neg_m);
+      float2 rs2[4], rq2[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) rs2[a] = rq2[a] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
@@ -367,17 +221,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int i = 0; i < 32; ++i) {
           const int c = (h * 64 + 2 * i) >> 5;
           const int e = (h * 64 + 2 * i) & 31;
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, neg_m));
-          const uint32_t u = pack_bf16x2(p0, p1);
-          rs += p0 + p1;
-          rq += __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
-          pk[i] = u;
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sl2x2, nm2);
+          const float p0 = ex2_approx(x.x);
+          const float p1 = ex2_approx(x.y);
+          const uint32_t pu = pack_bf16x2(p0, p1);
+          rs2[i & 3] = __fadd2_rn(rs2[i & 3], make_float2(p0, p1));
+          rq2[i & 3] = __fadd2_rn(rq2[i & 3], make_float2(__uint_as_float(pu << 16),
+                                                           __uint_as_float(pu & 0xffff0000u)));
+          pk[i] = pu;
         }
         tmem_st_32x32b_x32(tS + h * 32, pk);
       }
-      l = l * alpha + rs;
-      lq = lq * alpha + rq;
+      const float2 rs_a = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
+      const float2 rq_a = __fadd2_rn(__fadd2_rn(rq2[0], rq2[1]), __fadd2_rn(rq2[2], rq2[3]));
+      l = l * alpha + (rs_a.x + rs_a.y);
+      lq = lq * alpha + (rq_a.x + rq_a.y);
       // correction (after P, when the S registers are dead): rescale this row of
       // O when its reference max moved.  PV_{j-1} has completed: S_j was
       // committed after it.
@@ -395,20 +254,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(&bar.p_full[t]);
+      mbar_arrive(bar(L::kPFull + t));
     }
 
     // ---- epilogue: O / l → bf16 → smem (swizzled) → TMA store; lse
     if (nt > 0) {
       if (ok) {
-        ok = wait_bounded(&bar.o_full[t], 0, ctl, kSiteSoftO | t);
+        ok = wait_bounded(bar(L::kOFull + t), 0, ctl, kSiteSoftO | t);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {
         tc_fence_after_sync();
         const float inv_l = lq > 0.f ? 1.f / lq : 0.f;
-        uint8_t* stage = sQ + t * L::kTileBytes;  // Q_t is no longer read by any MMA
-        const uint32_t stage_addr = smem_u32(stage);
+        // Q_t's buffer is no longer read by any MMA: it stages this tile's output
+        const uint32_t stage = sb + L::kQOff + t * L::kTileBytes;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -420,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const int unit = c * 4 + q4;  // 16-byte unit index along the row
             const int chunk = unit >> 3;
             const int u16 = unit & 7;
-            const uint32_t addr = stage_addr + chunk * L::kChunkBytes + row * 128 +
+            const uint32_t addr = stage + chunk * L::kChunkBytes + row * 128 +
                                   ((u16 ^ (row & 7)) << 4);
             uint32_t w[4];
 #pragma unroll
@@ -433,19 +292,180 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+#pragma unroll
           for (int c = 0; c < L::kChunks; ++c)
             tma_store_3d(&p.tm_o, stage + c * L::kChunkBytes + wq * 32 * 128, c * 64,
                          qt * kBlockM + wq * 32, bh);
           tma_store_commit();
         }
-        if (grow < p.S) {
-          const float lse2 = m + __log2f(l);
-          p.lse[(int64_t)bh * p.S + grow] = lse2 * kLn2;
-        }
+        if (grow < p.S) p.lse[(int64_t)bh * p.S + grow] = (m + __log2f(l)) * kLn2;
         if (lane == 0) tma_store_wait_all();
       }
     }
     tc_fence_before_sync();
+  } else {
+    warpgroup_reg_release<kControlRegs>();
+    if (warp == 9 && lane == 0) {
+      // ======================= TMA producer =======================
+      const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_o);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if ((t == 0 ? n0 : n1) == 0) continue;
+        mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sb + L::kQOff + t * L::kTileBytes + c * L::kChunkBytes, &p.tm_q,
+                      bar(L::kQFull + t), c * 64, (t == 0 ? qt0 : qt1) * kBlockM, bh, pol_q);
+      }
+      int k_issued = 0, v_issued = 0;  // K / V tiles whose loads were issued
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        const int ks = j % L::kKStages;
+        ok = wait_bounded(bar(L::kKEmpty + ks), ((j / L::kKStages) & 1) ^ 1, ctl, kSiteProducerK | j);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::kKFull + ks), L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sb + L::kKOff + ks * L::kTileBytes + c * L::kChunkBytes, &p.tm_k,
+                      bar(L::kKFull + ks), c * 64, j * kBlockN, bh, pol_kv);
+        k_issued = j + 1;
+        const int vs = j % L::kVStages;
+        ok = wait_bounded(bar(L::kVEmpty + vs), ((j / L::kVStages) & 1) ^ 1, ctl, kSiteProducerV | j);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::kVFull + vs), L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sb + L::kVOff + vs * L::kTileBytes + c * L::kChunkBytes, &p.tm_v,
+                      bar(L::kVFull + vs), c * 64, j * kBlockN, bh, pol_kv);
+        v_issued = j + 1;
+      }
+      if (ok) {
+        // Tail: wait until the tensor core has released every stage, so that
+        // no commit-arrive on a ring barrier can land after this CTA is gone.
+        for (int j = max(nkv - L::kKStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(bar(L::kKEmpty + j % L::kKStages), (j / L::kKStages) & 1, ctl,
+                            kSiteProducerK | 0xff);
+        for (int j = max(nkv - L::kVStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(bar(L::kVEmpty + j % L::kVStages), (j / L::kVStages) & 1, ctl,
+                            kSiteProducerV | 0xff);
+      }
+      if (!ok) {
+        // Abort: let every copy this thread started land before leaving.  The
+        // last load into each stage completes its stage's latest full phase.
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if ((t == 0 ? n0 : n1) > 0) wait_drain(bar(L::kQFull + t), 0, kDrainLimitNs);
+        for (int j = max(k_issued - L::kKStages, 0); j < k_issued; ++j)
+          wait_drain(bar(L::kKFull + j % L::kKStages), (j / L::kKStages) & 1, kDrainLimitNs);
+        for (int j = max(v_issued - L::kVStages, 0); j < v_issued; ++j)
+          wait_drain(bar(L::kVFull + j % L::kVStages), (j / L::kVStages) & 1, kDrainLimitNs);
+      }
+    } else if (warp == 8) {
+      // ======================= tcgen05 issuer =======================
+      // The whole warp runs the schedule (so descriptors and loop state are
+      // warp-uniform); one elected lane issues every tcgen05.mma and commit.
+      const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
+      const bool leader = elect_one();
+      constexpr uint32_t kIdescS = instr_desc_bf16(kBlockM, kBlockN, false, false);
+      constexpr uint32_t kIdescO = instr_desc_bf16(kBlockM, D, false, true);
+      // Descriptor bases; a K step or a stage only moves the start-address
+      // field (16-byte units; no carry out of it: smem < 256 KB).
+      const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
+      const uint64_t dk = smem_desc_sw128(sb + L::kKOff, 16, 1024);
+      const uint64_t dv = smem_desc_sw128(sb + L::kVOff, L::kChunkBytes, 1024);
+      constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
+
+      // S_t = Q_t · K_stageᵀ: D/16 MMAs of K = 16 (32 bytes within a 128-byte
+      // swizzle row; the next 64 columns are the next 16 KB block).
+      auto issue_s = [&](int t, int ks) {
+        const uint64_t da = dq + t * kTileUnits;
+        const uint64_t db = dk + ks * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem_base + t * 128, da + off, db + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t · V_stage: 8 MMAs of K = 16 key rows (2 KB of V each).
+      auto issue_pv = [&](int t, int vs, bool accumulate) {
+        const uint64_t db = dv + vs * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts(tmem_base + 256 + t * D, tmem_base + t * 128 + kk * 8, db + (kk * (2048 >> 4)),
+                 kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+      };
+      auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
+        return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
+      };
+
+      bool ok = true;
+      if (n0 > 0) ok = wait_warp(bar(L::kQFull + 0), 0, kSiteMmaQ);
+      if (ok && n1 > 0) ok = wait_warp(bar(L::kQFull + 1), 0, kSiteMmaQ | 1);
+      if (ok) ok = wait_warp(bar(L::kKFull + 0), 0, kSiteMmaK);
+      if (ok) {
+        tc_fence_after_sync();
+        if (leader) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if ((t == 0 ? n0 : n1) == 0) continue;
+            issue_s(t, 0);
+            mma_commit(bar(L::kSFull + t));
+          }
+          mma_commit(bar(L::kKEmpty + 0));
+        }
+        __syncwarp();
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int vs = j % L::kVStages;
+          ok = wait_warp(bar(L::kVFull + vs), (j / L::kVStages) & 1, kSiteMmaV | j);
+          if (!ok) break;
+          const int kn = j + 1;
+          const int ksn = kn % L::kKStages;
+          bool k_next_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int ntt = t == 0 ? n0 : n1;
+            if (!ok || j >= ntt) continue;
+            ok = wait_warp(bar(L::kPFull + t), j & 1, kSiteMmaP | (t << 7) | j);
+            if (!ok) break;
+            tc_fence_after_sync();
+            if (leader) issue_pv(t, vs, j > 0);
+            if (kn < ntt) {
+              if (!k_next_ready) {
+                ok = wait_warp(bar(L::kKFull + ksn), (kn / L::kKStages) & 1, kSiteMmaK | kn);
+                if (!ok) break;
+                k_next_ready = true;
+                tc_fence_after_sync();
+              }
+              if (leader) {
+                issue_s(t, ksn);
+                mma_commit(bar(L::kSFull + t));
+              }
+            } else if (leader) {
+              mma_commit(bar(L::kOFull + t));
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          if (leader) {
+            mma_commit(bar(L::kVEmpty + vs));
+            if (k_next_ready) mma_commit(bar(L::kKEmpty + ksn));
+          }
+          __syncwarp();
+        }
+      }
+      // Every MMA the leader issued has completed once `drain` arrives.
+      if (leader) {
+        mma_commit(bar(L::kDrain));
+        wait_drain(bar(L::kDrain), 0, kDrainLimitNs);
+      }
+      __syncwarp();
+    }
   }
 
   __syncthreads();

@@ -29,8 +29,10 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // ---------------------------------------------------------------- mbarrier
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+// All shared-memory operands are 32-bit shared-window addresses (smem_u32);
+// pointer overloads are provided for convenience.
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
 // Makes barrier initialisation visible to the async proxy (TMA, tcgen05).
@@ -38,39 +40,70 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
-               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+               ::"r"(bar), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
-// Shared control block of one CTA: the abort flag every bounded wait polls.
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns` while
+// the phase is incomplete (it resumes as soon as the phase completes), so a
+// waiting warp does not take issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ int ld_volatile_shared(uint32_t addr) {
+  int v;
+  asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_volatile_shared(uint32_t addr, int v) {
+  asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// What a bounded wait needs: the CTA's abort flag (shared memory, non-zero
+// once any role gave up), the global status words, and the bound.
 struct WaitCtl {
-  volatile int* abort_flag;  // shared memory; non-zero once any role gave up
-  int* status;               // global status word (may be null)
-  uint64_t timeout_ns;       // bound on one wait
+  uint32_t abort_flag;  // shared-window address of an int
+  int* status;          // global status words [error bits, first wait site] (may be null)
+  uint64_t timeout_ns;  // bound on one wait
 };
+
+// Longest a bounded wait lets a thread sleep inside one try_wait (it wakes as
+// soon as the phase completes); the timeout and abort flag are checked between.
+constexpr uint32_t kSuspendHintNs = 200000;
 
 // Device status bits (combined with atomicOr in the global status word).
 enum : int { kStatusTimeout = 1 };
 
-__device__ __forceinline__ void raise_abort(const WaitCtl& c, int where) {
-  *c.abort_flag = 1;
+__device__ __noinline__ void raise_abort(const WaitCtl& c, int where) {
+  st_volatile_shared(c.abort_flag, 1);
   if (c.status != nullptr) {
     atomicOr(c.status, kStatusTimeout);
     atomicCAS(c.status + 1, 0, where);  // first place that gave up, for diagnosis
@@ -80,13 +113,13 @@ __device__ __forceinline__ void raise_abort(const WaitCtl& c, int where) {
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns false
 // if it did not complete within c.timeout_ns or if the CTA is aborting; in
 // the first case the abort is raised here.  `where` tags the wait site.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const WaitCtl& c,
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                              int where) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*c.abort_flag) return false;
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if (ld_volatile_shared(c.abort_flag)) return false;
     if (global_timer_ns() - t0 > c.timeout_ns) {
       raise_abort(c, where);
       return false;
@@ -96,12 +129,26 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
 
 // Wait used only while tearing down after an abort: ignores the abort flag,
 // bounded by its own limit.  Returns false if the limit ran out.
-__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
+}
+
+// pointer overloads
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) { mbar_init(smem_u32(bar), count); }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) { mbar_arrive(smem_u32(bar)); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  mbar_arrive_expect_tx(smem_u32(bar), bytes);
+}
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const WaitCtl& c,
+                                             int where) {
+  return wait_bounded(smem_u32(bar), parity, c, where);
+}
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return wait_drain(smem_u32(bar), parity, limit_ns);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -110,21 +157,25 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 }
 
 // 3-D tiled load global → shared, completion counted in bytes on `bar`.
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
                                             int y, int z, uint64_t cache_policy) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4, %5}], [%2], %6;"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y),
-        "r"(z), "l"(cache_policy)
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z),
+        "l"(cache_policy)
       : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y, int z, uint64_t cache_policy) {
+  tma_load_3d(smem_u32(dst), map, smem_u32(bar), x, y, z, cache_policy);
 }
 
 // 3-D tiled store shared → global (rows outside the tensor are not written).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
                                              int z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
 
@@ -156,9 +207,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 
 // ---------------------------------------------------------------- tcgen05
 // Tensor-memory allocation (whole warp).  The TMEM address is written to smem.
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-               ::"r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+               ::"r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  tmem_alloc(smem_u32(dst_smem), ncols);
 }
 
 __device__ __forceinline__ void tmem_relinquish() {
@@ -202,10 +256,11 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               ::"r"(smem_u32(bar)) : "memory");
+               ::"r"(bar) : "memory");
 }
+__device__ __forceinline__ void mma_commit(uint64_t* bar) { mma_commit(smem_u32(bar)); }
 
 // 32 lanes x 32 bits, 32 consecutive columns: thread t of the warp gets
 // lane (lane field of taddr + t), columns col .. col+31.
@@ -250,7 +305,35 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
+// One lane of the (fully active) warp is elected; the same lane every time.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(r));
+  return r != 0;
+}
+
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register budget (all four warps of the warpgroup execute it).
+template <uint32_t N>
+__device__ __forceinline__ void warpgroup_reg_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void warpgroup_reg_acquire() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- misc
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(160, 1) umma_unit_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  WaitCtl ctl{abort_flag, p.status, 1000000000ull};
+  WaitCtl ctl{smem_u32(const_cast<int*>(abort_flag)), p.status, 1000000000ull};
 
   if (warp == 4) {
     if (lane == 0) {
