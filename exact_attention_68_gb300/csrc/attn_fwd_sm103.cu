@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     float m = -INFINITY;  // running max of scale·log2e·s (log2 domain), possibly stale
     float l = 0.f;        // running sum of p = 2^(t - m) in fp32: gives the logsumexp
-    float lq = 0.f;       // running sum of p rounded to bf16, the weights the tensor
-                          // core multiplies V by: normalises the output, so that
-                          // the rounding of P cancels between numerator and denominator
+    float lq = 0.f;       // l plus, for each tile, the bf16 rounding error of the tile's
+                          // largest p: normalises the output, so that a row dominated
+                          // by one key is weighted exactly as the tensor core weights it
+    bool moved_before = false;  // the reference max moved in this warp's previous tile
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       ok = wait_bounded(bar(L::kSFull + t), j & 1, ctl, kSiteSoftS | (t << 7) | j);
@@ -165,57 +166,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!ok) break;
       tc_fence_after_sync();
 
+      // S_j arrives in two 64-column halves: the second half's TMEM load is in
+      // flight while the first half is processed.
       uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + c * 32, sr[c]);
+      tmem_ld_32x32b_x32(tS + 0, sr[0]);
+      tmem_ld_32x32b_x32(tS + 32, sr[1]);
       tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+      reg_fence(sr[0]);
+      reg_fence(sr[1]);
+      tmem_ld_32x32b_x32(tS + 64, sr[2]);
+      tmem_ld_32x32b_x32(tS + 96, sr[3]);
 
       // mask: key column > query row (causal diagonal tile) or column >= S (tail)
       const bool edge = (CAUSAL && j == qt) || ((j + 1) * kBlockN > p.S);
-      if (edge) {
-        int lim = p.S - 1 - j * kBlockN;  // last allowed column inside this tile
-        if (CAUSAL) lim = min(lim, grow - j * kBlockN);
+      int lim = p.S - 1 - j * kBlockN;  // last allowed column inside this tile
+      if (CAUSAL) lim = min(lim, grow - j * kBlockN);
+      auto mask_half = [&](int h) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 2 * h; c < 2 * h + 2; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (c * 32 + i > lim) sr[c][i] = __float_as_uint(-INFINITY);
-      }
-
-      // row max: 16 independent three-input chains of 8 scores, then a tree
-      float cm[16];
+      };
+      // max of one 64-column half: 8 independent three-input chains, then a tree
+      auto max_half = [&](int h) -> float {
+        float cm[8];
 #pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        const uint32_t* e = &sr[g >> 2][(g & 3) * 8];
-        float a = max3f(__uint_as_float(e[0]), __uint_as_float(e[1]), __uint_as_float(e[2]));
-        a = max3f(a, __uint_as_float(e[3]), __uint_as_float(e[4]));
-        a = max3f(a, __uint_as_float(e[5]), __uint_as_float(e[6]));
-        cm[g] = fmaxf(a, __uint_as_float(e[7]));
-      }
-      const float mx = fmaxf(max3f(max3f(cm[0], cm[1], cm[2]), max3f(cm[3], cm[4], cm[5]),
-                                   max3f(cm[6], cm[7], cm[8])),
-                             max3f(max3f(cm[9], cm[10], cm[11]), max3f(cm[12], cm[13], cm[14]),
-                                   cm[15]));
-      const float m_new = fmaxf(m, mx * sl2);
-      float alpha = 1.f;
-      if (j == 0) {
-        m = m_new;
-      } else if (m_new > m + kRescaleThreshold) {
-        alpha = ex2_approx(m - m_new);
-        m = m_new;
-      }
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      // p = 2^(s·scale·log2e − m), two scores per packed FMA; four independent
-      // packed accumulators for each of the two row sums
-      const float2 sl2x2 = make_float2(sl2, sl2);
-      const float2 nm2 = make_float2(neg_m, neg_m);
-      float2 rs2[4], rq2[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) rs2[a] = rq2[a] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t* e = &sr[2 * h + (g >> 2)][(g & 3) * 8];
+          float a = max3f(__uint_as_float(e[0]), __uint_as_float(e[1]), __uint_as_float(e[2]));
+          a = max3f(a, __uint_as_float(e[3]), __uint_as_float(e[4]));
+          a = max3f(a, __uint_as_float(e[5]), __uint_as_float(e[6]));
+          cm[g] = fmaxf(a, __uint_as_float(e[7]));
+        }
+        return fmaxf(max3f(cm[0], cm[1], cm[2]), max3f(max3f(cm[3], cm[4], cm[5]), cm[6], cm[7]));
+      };
+      // p = 2^(s·scale·log2e − m) for one half, two scores per packed FMA; P
+      // (bf16) goes to TMEM over the consumed S columns; four packed
+      // accumulators for the row sum.
+      float2 rs2[4];
+      auto exp_half = [&](int h, float neg_m) {
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 nm2 = make_float2(neg_m, neg_m);
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -225,22 +217,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sl2x2, nm2);
           const float p0 = ex2_approx(x.x);
           const float p1 = ex2_approx(x.y);
-          const uint32_t pu = pack_bf16x2(p0, p1);
           rs2[i & 3] = __fadd2_rn(rs2[i & 3], make_float2(p0, p1));
-          rq2[i & 3] = __fadd2_rn(rq2[i & 3], make_float2(__uint_as_float(pu << 16),
-                                                           __uint_as_float(pu & 0xffff0000u)));
-          pk[i] = pu;
+          pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st_32x32b_x32(tS + h * 32, pk);
+      };
+      auto clear_sums = [&]() {
+#pragma unroll
+        for (int a = 0; a < 4; ++a) rs2[a] = make_float2(0.f, 0.f);
+      };
+
+      // From the second tile on, unless the previous tile moved it, the
+      // exponentials are computed against the current reference max right away
+      // (it only moves when a row's max grows by more than the threshold); the
+      // row max is checked alongside, and a tile that moves it is redone.
+      const bool speculate = j > 0 && !moved_before;
+      clear_sums();
+      if (edge) mask_half(0);
+      const float mx0 = max_half(0);
+      if (speculate) exp_half(0, -m);
+      tmem_ld_wait();
+      reg_fence(sr[2]);
+      reg_fence(sr[3]);
+      if (edge) mask_half(1);
+      const float mx = fmaxf(mx0, max_half(1));  // this row's largest raw score in the tile
+      const float m_tile = mx * sl2;
+      if (speculate) exp_half(1, -m);
+      float alpha = 1.f;
+      bool moved = false;
+      if (j == 0) {
+        m = m_tile;  // first tile: the reference is this tile's max
+      } else if (m_tile > m + kRescaleThreshold) {
+        alpha = ex2_approx(m - m_tile);
+        m = m_tile;
+        moved = true;
+      }
+      moved_before = __any_sync(0xffffffffu, moved);
+      if (!speculate || moved_before) {
+        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        clear_sums();
+        exp_half(0, neg_m);
+        exp_half(1, neg_m);
       }
       const float2 rs_a = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
-      const float2 rq_a = __fadd2_rn(__fadd2_rn(rq2[0], rq2[1]), __fadd2_rn(rq2[2], rq2[3]));
-      l = l * alpha + (rs_a.x + rs_a.y);
-      lq = lq * alpha + (rq_a.x + rq_a.y);
-      // correction (after P, when the S registers are dead): rescale this row of
-      // O when its reference max moved.  PV_{j-1} has completed: S_j was
-      // committed after it.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      const float rs = rs_a.x + rs_a.y;
+      // the tile's largest p, computed exactly as in P, and its bf16 value
+      const float pmax = ex2_approx(fmaf(mx, sl2, (m == -INFINITY) ? 0.f : -m));
+      const float pmax_q = __uint_as_float(pack_bf16x2(pmax, 0.f) << 16);
+      l = l * alpha + rs;
+      lq = lq * alpha + (rs + (pmax_q - pmax));
+      // correction: rescale this row of O when its reference max moved.  PV_{j-1}
+      // has completed: S_j was committed after it.
+      if (moved_before) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
