@@ -20,6 +20,8 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIBDIR, "libattn_sm103.so")
 UNIT_SRC = os.path.join(ROOT, "tests", "cuda", "umma_unit.cu")
 UNIT_LIB = os.path.join(ROOT, "tests", "cuda", "libumma_unit.so")
+SCHED_SRC = os.path.join(ROOT, "tests", "cuda", "sched_check.cpp")
+SCHED_LIB = os.path.join(ROOT, "tests", "cuda", "libsched_check.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
@@ -80,7 +82,20 @@ def build_unit_library(force: bool = False, verbose: bool = False) -> str:
     return UNIT_LIB
 
 
+def build_sched_check(force: bool = False, verbose: bool = False) -> str:
+    """Build the test-only host shim over the grid schedule (g++, no CUDA)."""
+    hdr = os.path.join(CSRC, "schedule.h")
+    if force or _stale(SCHED_LIB, [hdr, SCHED_SRC]):
+        tmp = SCHED_LIB + ".tmp"
+        cxx = os.environ.get("CXX") or shutil.which("g++") or "g++"
+        _run([cxx, "-O2", "-std=c++17", "-fPIC", "-shared", "-fvisibility=hidden",
+              "-I", CSRC, "-o", tmp, SCHED_SRC], verbose)
+        os.replace(tmp, SCHED_LIB)
+    return SCHED_LIB
+
+
 if __name__ == "__main__":
     force = "--force" in sys.argv
     print(build_library(force=force, verbose=True))
     print(build_unit_library(force=force, verbose=True))
+    print(build_sched_check(force=force, verbose=True))

@@ -9,7 +9,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "attn_fwd.h"
 #include "attn_host.h"
 #include "tmap.h"
@@ -17,6 +17,9 @@
 namespace {
 
 constexpr uint64_t kDefaultWaitTimeoutNs = 2000000000ull;  // 2 s per in-kernel wait
+// K/V bytes of the (b, h) slices one scheduling group spans: well under the
+// 129 MB L2, so that the CTAs running at one time re-read K/V tiles from L2.
+constexpr int64_t kL2GroupBytes = 48ll << 20;
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
@@ -132,6 +135,11 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
   p.S = static_cast<int>(S);
   p.n_qt = static_cast<int>((S + kBlockM - 1) / kBlockM);
   p.n_units = (p.n_qt + kQTilesPerUnit - 1) / kQTilesPerUnit;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  p.sched = plan_schedule(BH, p.n_units, S, D, causal != 0, kL2GroupBytes, sms);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout_ns;
   if (fwd_launch(p, static_cast<int>(D), causal != 0, stream) != cudaSuccess) {

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include "schedule.h"
+
 namespace ea {
 
 // Rows of one Q tile (the tcgen05 M) and of one K/V tile.
@@ -32,6 +34,7 @@ struct FwdParams {
   int B, H, S;
   int n_qt;          // ceil(S / 128)
   int n_units;       // ceil(n_qt / 2): work units per (b, h)
+  UnitSchedule sched;  // CTA index -> (b·H + h, unit level)
   float scale_log2;  // scale · log2(e)
   uint64_t timeout_ns;
 };

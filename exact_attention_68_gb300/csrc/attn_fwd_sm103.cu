@@ -96,11 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit: (b·H + h, pair of Q tiles), heaviest units first
-  const int BH = p.B * p.H;
-  const int unit_rev = blockIdx.x / BH;
-  const int bh = blockIdx.x - unit_rev * BH;
-  const int u = p.n_units - 1 - unit_rev;
+  // ---- work unit: (b·H + h, pair of Q tiles), from the grid schedule
+  int bh, u;
+  schedule_unit(p.sched, static_cast<int>(blockIdx.x), &bh, &u);
   const int qt0 = 2 * u;
   const int qt1 = 2 * u + 1;
   const int n0 = CAUSAL ? qt0 + 1 : p.n_qt;

@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime_api.h>
 
-#include "../../include/attn.h"
+#include "attn.h"
 
 namespace ea {
 

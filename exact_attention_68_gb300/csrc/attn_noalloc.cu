@@ -22,7 +22,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "attn_host.h"
 
 namespace {

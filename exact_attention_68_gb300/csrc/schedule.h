@@ -1,0 +1,82 @@
+// schedule.h — which work unit each CTA of the forward kernel's 1-D grid takes.
+//
+// A work unit is one (b·H + h) slice and one pair of 128-row Q tiles, unit
+// level u covering Q tiles 2u and 2u+1.  Under the causal mask level u does
+// 2u+2 KV tile-steps, so the levels differ in cost and the order of the grid
+// decides both the load balance and how often K/V tiles come back from DRAM:
+//
+//   phase 1  levels n_units-1 .. tail_levels, one group of heads_per_group
+//            slices at a time; within a group the levels go heaviest first and
+//            the slices of a level sit side by side.  One group's K/V is sized
+//            to stay in L2, so the CTAs in flight re-read tiles from L2.
+//   phase 2  levels tail_levels-1 .. 0 over all slices, heaviest first: the
+//            light units that even out the finish times of the SMs.
+//
+// Host and device share this mapping; it is a bijection from
+// [0, BH·n_units) onto (slice, level) pairs.
+#pragma once
+
+#include <cstdint>
+
+#ifdef __CUDACC__
+#define EA_HOST_DEVICE __host__ __device__ __forceinline__
+#else
+#define EA_HOST_DEVICE inline
+#endif
+
+namespace ea {
+
+struct UnitSchedule {
+  int BH;               // B·H slices
+  int n_units;          // unit levels per slice
+  int heads_per_group;  // slices per group in phase 1 (>= 1)
+  int tail_levels;      // levels run in phase 2, 0 .. n_units
+};
+
+// CTA index x in [0, BH·n_units) -> slice *bh and unit level *u.
+EA_HOST_DEVICE void schedule_unit(const UnitSchedule& s, int x, int* bh, int* u) {
+  const int grouped_levels = s.n_units - s.tail_levels;
+  const int phase1 = s.BH * grouped_levels;
+  if (x < phase1) {
+    const int per_group = s.heads_per_group * grouped_levels;
+    const int group = x / per_group;
+    const int g0 = group * s.heads_per_group;
+    const int rest = s.BH - g0;
+    const int g_size = s.heads_per_group < rest ? s.heads_per_group : rest;
+    const int r = x - group * per_group;
+    const int level_rev = r / g_size;
+    *bh = g0 + (r - level_rev * g_size);
+    *u = s.n_units - 1 - level_rev;
+  } else {
+    const int y = x - phase1;
+    const int level_rev = y / s.BH;
+    *bh = y - level_rev * s.BH;
+    *u = s.tail_levels - 1 - level_rev;
+  }
+}
+
+// Host choice of the schedule.  kv_group_bytes: K/V bytes one group may span;
+// sms: the device's SM count.  Phase 2 gets about sqrt(2·n_units·sms/BH)
+// levels: per SM roughly the cost of one of the heaviest units, which is the
+// spread of finish times phase 1 can leave.  Without the causal mask every
+// unit costs the same and phase 2 is empty.
+inline UnitSchedule plan_schedule(int64_t BH, int64_t n_units, int64_t S, int64_t D, bool causal,
+                                  int64_t kv_group_bytes, int sms) {
+  UnitSchedule s;
+  s.BH = static_cast<int>(BH);
+  s.n_units = static_cast<int>(n_units);
+  const int64_t kv_bytes = S * D * 2 * 2;  // K and V of one slice, bf16
+  int64_t g = kv_group_bytes / kv_bytes;
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  s.heads_per_group = static_cast<int>(g);
+  int64_t tail = 0;
+  if (causal) {
+    const int64_t want = 2 * n_units * (sms > 0 ? sms : 1);
+    while (tail < n_units && tail * tail * BH < want) ++tail;
+  }
+  s.tail_levels = static_cast<int>(tail);
+  return s;
+}
+
+}  // namespace ea

@@ -34,6 +34,28 @@ def test_workload_parity(cuda_device, name):
     print(name, s)
 
 
+
+@pytest.mark.parametrize("S,D", [(4096, 128), (8192, 64)])
+def test_ragged_head_groups(cuda_device, S, D):
+    """(b, h) slices are scheduled in groups whose K/V fit in L2 (24 slices
+    here); 40 slices do not divide into them evenly.  Rows 0, 127, 128, S-1 of
+    every slice, every row of the last slice and 512 rows drawn by
+    default_rng(3) are compared."""
+    B, H = 2, 20
+    q, k, v = make_qkv((B, H, S, D), seed=13)
+    scale = default_scale(D)
+    out, lse = run_gpu(q, k, v, scale, True)
+    rows = [(b, h, i) for b in range(B) for h in range(H) for i in (0, 127, 128, S - 1)]
+    rows += [(B - 1, H - 1, i) for i in range(S)]
+    rng = np.random.default_rng(3)
+    rows += [(int(b), int(h), int(i)) for b, h, i in
+             zip(rng.integers(0, B, 512), rng.integers(0, H, 512), rng.integers(0, S, 512))]
+    idx = np.asarray(rows, dtype=np.int64)
+    ro, rl = _oracle_rows(q, k, v, scale, True, idx)
+    og = to_f64(out)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    lg = to_f64(lse)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    compare(og, lg, ro, rl, f"ragged groups S={S} D={D}")
+
 EDGE_SHAPES = [
     (1, 1, 1, 64), (1, 1, 1, 128), (1, 1, 7, 64), (1, 1, 7, 128), (2, 3, 129, 64),
     (1, 2, 200, 128), (1, 1, 256, 128), (1, 1, 384, 64), (3, 1, 1000, 128), (1, 2, 640, 64),
