@@ -44,16 +44,20 @@ KERNEL_SOURCES = ["exact_attention_68_gb300/csrc/attn_fwd_sm103.cu",
 # were taken on (a changed kernel reports null until captured again).
 NCU_TRAFFIC_BYTES = {
     # B=1 H=32 S=16384 D=128 causal: 807,346,688 read + 113,161,216 written
-    "8bbd910acfd709f6": 920507904,
+    "ed9f7a1036cc7891": 920507904,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 def kernel_hash() -> str:
+    """Hash of the kernel sources with // comments and blank lines left out."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
@@ -209,15 +213,39 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def time_steps(fn, steps, stream):
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+def time_steps(fn, steps, stream, per_step=False):
+    """Total ms of `steps` calls between two events on `stream`; with per_step,
+    also an event after every call and the per-call durations (ms)."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1 if per_step else 2)]
     torch.cuda.synchronize()
-    start.record(stream)
-    for _ in range(steps):
+    ev[0].record(stream)
+    for i in range(steps):
         fn()
-    end.record(stream)
-    end.synchronize()
-    return start.elapsed_time(end)  # ms
+        if per_step:
+            ev[i + 1].record(stream)
+    if not per_step:
+        ev[1].record(stream)
+    ev[-1].synchronize()
+    total = ev[0].elapsed_time(ev[-1])
+    if not per_step:
+        return total
+    return total, [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
+def executed_flops(B, H, S, D, causal):
+    """FLOPs of the 128x128 tiles the kernel actually runs (diagonal tiles whole)."""
+    n = (S + 127) // 128
+    tiles = n * (n + 1) // 2 if causal else n * n
+    return 4 * B * H * tiles * 128 * 128 * D
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((i.get("num_threads", 0) for i in threadpool_info()), default=None)
+    except Exception:
+        v = os.environ.get("OMP_NUM_THREADS")
+        return int(v) if v and v.isdigit() else None
 
 
 def side_workloads(device, stream):
@@ -284,7 +312,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
-    ms = time_steps(step, args.steps, stream)
+    ms, per_launch = time_steps(step, args.steps, stream, per_step=True)
     t1 = time.time()
     torch.cuda.synchronize()
     barrier(world)
@@ -321,7 +349,8 @@ def run_ours(args, world, rank, local):
         tf, n_rows, secs = oracle_rows_sample(*as_numpy(q_h, k_h, v_h), scale, w.causal, 256,
                                               list(range(w.H)), args.cpu_budget)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-               "kind": "oracle",
+               "kind": "oracle", "blas_threads": blas_threads(),
+               "full_problem_s_extrapolated": flops / (tf * 1e12),
                "sample": f"{n_rows} query rows (256 evenly spaced per head, heads in order) of the "
                          f"{w.about} workload, oracle row form in fp64 numpy, {secs:.1f} s"}
     if rank != 0:
@@ -336,6 +365,9 @@ def run_ours(args, world, rank, local):
                    "l2": "inputs 403 MB > 129 MB L2: no flush between steps",
                    "parallelism": f"replicas x{world} (independent (b,h) shards)"},
         "pct_of_peak": 100.0 * achieved / peak,
+        "ms_per_launch": {"mean": ms_max / args.steps, "median": statistics.median(per_launch),
+                          "min": min(per_launch), "max": max(per_launch)},
+        "executed_over_counted_flops": executed_flops(w.B, w.H, w.S, w.D, w.causal) / flops,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",

@@ -18,7 +18,8 @@
 //   warps 0-3   softmax/correction/epilogue for Q tile 0 (rows 0-127 of the unit)
 //   warps 4-7   the same for Q tile 1 (rows 128-255).  One thread owns one query
 //               row (its TMEM lane): row max and row sums need no shuffles.
-//   warp 8      tcgen05 issuer (one thread): S_t = Q_t·K_jᵀ (A, B from smem) and
+//   warp 8      tcgen05 issuer (the warp waits together, one elected lane
+//               issues): S_t = Q_t·K_jᵀ (A, B from smem) and
 //               O_t += P_t·V_j (A = P from TMEM, B = V from smem, MN-major),
 //               fp32 accumulators in TMEM; completion signalled by
 //               tcgen05.commit on mbarriers.  Also owns the TMEM allocation.
@@ -31,6 +32,9 @@
 //
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
 // P_t (bf16, two per 32-bit column) overwrites columns [0,64) of S_t.
+//
+// Grid: one CTA per work unit, in the order schedule.h sets out (heavy causal
+// levels by L2-sized groups of heads, then the light levels over all heads).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
