@@ -233,3 +233,68 @@ def test_rows_form_equals_full_form():
         ro, rl = attention_rows(q, k, v, 0.3, causal, idx)
         np.testing.assert_array_equal(ro, out[idx[:, 0], idx[:, 1], idx[:, 2]])
         np.testing.assert_array_equal(rl, lse[idx[:, 0], idx[:, 1], idx[:, 2]])
+
+
+# ------------------------------------------------------------------ planted mistakes
+# Forward variants with one plausible slip each; every one must fail at least
+# one of the pins above (the golden examples, the brute force, torch's SDPA,
+# the first causal row, finiteness at large logits).
+
+
+def _fwd_mutant(kind):
+    def fwd(q, k, v, scale, causal):
+        q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+        B, H, S, D = q.shape
+        out = np.empty_like(q)
+        lse = np.empty((B, H, S))
+        for b in range(B):
+            for h in range(H):
+                kh = k[b, h][::-1] if kind == "k_reversed" else k[b, h]
+                vh = v[b, h][::-1] if kind == "v_reversed" else v[b, h]
+                s = q[b, h] @ kh.T
+                if kind != "scale_dropped":
+                    s = s * scale
+                if causal:
+                    i, j = np.arange(S)[:, None], np.arange(S)[None, :]
+                    s = np.where((j < i) if kind == "mask_reversed" else (j > i), -np.inf, s)
+                m = 0.0 if kind == "no_max_shift" else np.max(s, axis=1, keepdims=True)
+                with np.errstate(over="ignore", invalid="ignore"):
+                    p = np.exp(s - m)
+                    l = p.sum(axis=1, keepdims=True)
+                    out[b, h] = (p / l) @ vh
+                    lse[b, h] = ((m + (np.log2(l) if kind == "lse_log2" else np.log(l)))[:, 0])
+        return out, lse
+    return fwd
+
+
+def _fwd_pins(fwd):
+    """The forward pins as checks over an implementation; False if any fails."""
+    for name in ("hand_worked_s3_d2.txt", "hand_worked_peaked_s2_d1.txt"):
+        g = _load_golden(name)
+        for causal, tag in ((True, "causal"), (False, "noncausal")):
+            out, lse = fwd(_bhsd(g["q"]), _bhsd(g["k"]), _bhsd(g["v"]), g["scale"], causal)
+            if not (np.allclose(out[0, 0], np.asarray(g[tag + "_out"], float), atol=1e-12)
+                    and np.allclose(lse[0, 0], np.asarray(g[tag + "_lse"], float), atol=1e-12)):
+                return False
+    rng = np.random.default_rng(31)
+    q, k, v = (_rand(rng, (1, 2, 6, 3), 2.0) for _ in range(3))
+    for causal in (True, False):
+        out, lse = fwd(q, k, v, 0.6, causal)
+        bo, bl = attention_fwd_loops(q.tolist(), k.tolist(), v.tolist(), 0.6, causal)
+        if not (np.allclose(out, np.asarray(bo), atol=1e-12) and np.allclose(lse, np.asarray(bl), atol=1e-12)):
+            return False
+    return True
+
+
+_FWD_MUTANTS = ["mask_reversed", "scale_dropped", "k_reversed", "v_reversed", "lse_log2",
+                "no_max_shift"]
+
+
+def test_forward_mutant_harness_unmutated_passes():
+    assert _fwd_pins(_fwd_mutant("none"))
+    assert _fwd_pins(attention_fwd)
+
+
+@pytest.mark.parametrize("kind", _FWD_MUTANTS)
+def test_forward_planted_mistake_fails_a_pin(kind):
+    assert not _fwd_pins(_fwd_mutant(kind)), kind
