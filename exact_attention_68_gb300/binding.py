@@ -18,7 +18,7 @@ import torch
 from .build import LIB_PATH
 
 __all__ = ["AttnError", "load_library", "attn_fwd", "attn_fwd_bounded", "attn_fwd_staged",
-           "attn_fwd_noalloc", "device_status", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
+           "attn_fwd_noalloc", "attn_bwd", "attn_bwd_bounded", "device_status", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
            "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
@@ -31,6 +31,8 @@ _SIGS = {
                              _i64, _i64, _i64, _i64, _f, _i, _p]),
     "attn_fwd_bounded": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _f, _i, _u64, _p]),
     "attn_fwd_noalloc": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _f, _i, _i, _p]),
+    "attn_bwd": (_i, [_p] * 10 + [_i64, _i64, _i64, _i64, _f, _i, _p]),
+    "attn_bwd_bounded": (_i, [_p] * 10 + [_i64, _i64, _i64, _i64, _f, _i, _u64, _p]),
     "attn_device_status": (_i, [_p]),
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_abi_version": (_i, []),
@@ -172,6 +174,50 @@ def attn_fwd_noalloc(q, k, v, out, lse, scale=None, causal=True, check_status=Tr
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_noalloc")
     return out, lse
+
+
+def attn_bwd(q, k, v, out, lse, dout, scale=None, causal=True, dq=None, dk=None, dv=None,
+             delta=None, stream=None):
+    """Gradient of attn_fwd.  Returns (dq, dk, dv) bf16 [B,H,S,D] and delta fp32 [B,H,S]."""
+    return attn_bwd_bounded(q, k, v, out, lse, dout, scale, causal, dq, dk, dv, delta, stream, None)
+
+
+def attn_bwd_bounded(q, k, v, out, lse, dout, scale=None, causal=True, dq=None, dk=None, dv=None,
+                     delta=None, stream=None, wait_timeout_ns: int | None = None):
+    """attn_bwd with an explicit bound on every in-kernel wait (None = library default)."""
+    _check_qkv(q, k, v)
+    B, H, S, D = q.shape
+    for name, t in (("out", out), ("dout", dout)):
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.shape != q.shape
+                or not t.is_contiguous() or t.device != q.device):
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q on its device")
+    if (not isinstance(lse, torch.Tensor) or lse.dtype != torch.float32 or lse.shape != (B, H, S)
+            or not lse.is_contiguous() or lse.device != q.device):
+        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    delta = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if delta is None else delta
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t.dtype != torch.bfloat16 or t.shape != q.shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if delta.dtype != torch.float32 or delta.shape != (B, H, S) or not delta.is_contiguous():
+        raise ValueError("delta must be a contiguous fp32 [B, H, S] tensor")
+    lib = load_library()
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(),
+            B, H, S, D, float(scale), 1 if causal else 0)
+    with torch.cuda.device(q.device):
+        st = _stream_handle(q.device, stream)
+        if wait_timeout_ns is None:
+            rc = lib.attn_bwd(*args, st)
+        else:
+            rc = lib.attn_bwd_bounded(*args, int(wait_timeout_ns), st)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv, delta
 
 
 def device_status(device=None, stream=None) -> int:

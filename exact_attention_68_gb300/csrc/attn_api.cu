@@ -116,6 +116,15 @@ attn_status_t validate_args(const void* q, const void* k, const void* v, const v
   return validate(q, k, v, out, lse, B, H, S, D, scale, causal);
 }
 
+attn_status_t current_status_words(int** status) {
+  int dev = -1;
+  DeviceState* st = nullptr;
+  attn_status_t s = device_state(&dev, &st);
+  if (s != ATTN_OK) return s;
+  *status = st->status;
+  return ATTN_OK;
+}
+
 attn_status_t launch_with_status(const void* q, const void* k, const void* v, void* out,
                                  float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
                                  float scale, int causal, uint64_t timeout_ns, int* status,

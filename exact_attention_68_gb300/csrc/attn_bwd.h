@@ -1,0 +1,40 @@
+// attn_bwd.h — parameters and launch entry of the attention backward kernels,
+// shared by the host API and the kernel translation unit (no device code).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace ea {
+
+// Both backward kernels: warps 0-7 elementwise (two groups of four warps, one
+// per half of a tile's 128 columns), warp 8 tcgen05 issuer, warp 9 producer.
+constexpr int kBwdThreads = 320;
+
+struct BwdParams {
+  CUtensorMap tm_q;   // q as (D, S, B·H), box 64 x 128 rows, 128-byte swizzle
+  CUtensorMap tm_k;   // k, same box
+  CUtensorMap tm_v;   // v, same box
+  CUtensorMap tm_do;  // dout, same box
+  CUtensorMap tm_dq;  // dq, box 64 x 32 rows (one warp's rows)
+  CUtensorMap tm_dk;  // dk, same
+  CUtensorMap tm_dv;  // dv, same
+  const uint16_t* out;   // bf16 [B·H, S, D]: forward output (rows read for delta)
+  const uint16_t* dout;  // bf16 [B·H, S, D]
+  const float* lse;      // [B·H, S]: natural-log logsumexp saved by the forward
+  float* delta;          // [B·H, S]: rowsum(dout ⊙ out), written by the dq kernel
+  int* status;           // device status word pair (error bits, first wait site)
+  int BH, S;
+  int n_t;               // ceil(S / 128): tiles along the sequence
+  float scale;           // softmax scale
+  float scale_log2;      // scale · log2(e)
+  uint64_t timeout_ns;
+};
+
+// Launches the dq kernel (which also writes delta) and then the dk/dv kernel
+// on `stream`.
+cudaError_t bwd_launch(const BwdParams& p, int D, bool causal, cudaStream_t stream);
+
+}  // namespace ea

@@ -1,0 +1,104 @@
+// attn_bwd_api.cu — the backward entry points of the C ABI declared in
+// include/attn.h: argument validation, tensor maps, launch of the two kernels.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "attn.h"
+#include "attn_bwd.h"
+#include "attn_host.h"
+#include "tmap.h"
+
+namespace {
+
+constexpr uint64_t kDefaultWaitTimeoutNs = 2000000000ull;  // 2 s per in-kernel wait
+
+bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Checks of attn_bwd; touches no CUDA API.
+attn_status_t validate_bwd(const void* q, const void* k, const void* v, const void* out,
+                           const float* lse, const void* dout, const void* dq, const void* dk,
+                           const void* dv, const float* delta, int64_t B, int64_t H, int64_t S,
+                           int64_t D, float scale, int causal) {
+  // shapes, scale, mask flag, q/k/v/out/lse pointers and alignment
+  attn_status_t s = ea::validate_args(q, k, v, out, lse, B, H, S, D, scale, causal);
+  if (s != ATTN_OK) return s;
+  if (!dout || !dq || !dk || !dv || !delta) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+       reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u)
+    return ATTN_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(delta) & 3u) return ATTN_ERR_MISALIGNED;
+  const uint64_t nt = static_cast<uint64_t>(B * H * S * D * 2);
+  const uint64_t nl = static_cast<uint64_t>(B * H * S * 4);
+  const void* ins[6] = {q, k, v, out, lse, dout};
+  const uint64_t in_bytes[6] = {nt, nt, nt, nt, nl, nt};
+  const void* outs[4] = {dq, dk, dv, delta};
+  const uint64_t out_bytes[4] = {nt, nt, nt, nl};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b])) return ATTN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_bwd_bounded(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               float* delta, int64_t B, int64_t H, int64_t S, int64_t D,
+                               float scale, int causal, uint64_t wait_timeout_ns,
+                               cudaStream_t stream) {
+  attn_status_t s = validate_bwd(q, k, v, out, lse, dout, dq, dk, dv, delta, B, H, S, D, scale,
+                                 causal);
+  if (s != ATTN_OK) return s;
+  int* status = nullptr;
+  s = ea::current_status_words(&status);
+  if (s != ATTN_OK) return s;
+  ea::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int64_t BH = B * H;
+  if (!ea::encode_bhsd_bf16(&p.tm_q, q, BH, S, D, 128) ||
+      !ea::encode_bhsd_bf16(&p.tm_k, k, BH, S, D, 128) ||
+      !ea::encode_bhsd_bf16(&p.tm_v, v, BH, S, D, 128) ||
+      !ea::encode_bhsd_bf16(&p.tm_do, dout, BH, S, D, 128) ||
+      !ea::encode_bhsd_bf16(&p.tm_dq, dq, BH, S, D, 32) ||
+      !ea::encode_bhsd_bf16(&p.tm_dk, dk, BH, S, D, 32) ||
+      !ea::encode_bhsd_bf16(&p.tm_dv, dv, BH, S, D, 32))
+    return ATTN_ERR_CUDA;
+  p.out = static_cast<const uint16_t*>(out);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.lse = lse;
+  p.delta = delta;
+  p.status = status;
+  p.BH = static_cast<int>(BH);
+  p.S = static_cast<int>(S);
+  p.n_t = static_cast<int>((S + 127) / 128);
+  if (static_cast<int64_t>(p.BH) * p.n_t > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.timeout_ns = wait_timeout_ns;
+  if (ea::bwd_launch(p, static_cast<int>(D), causal != 0, stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       float* delta, int64_t B, int64_t H, int64_t S, int64_t D, float scale,
+                       int causal, cudaStream_t stream) {
+  return attn_bwd_bounded(q, k, v, out, lse, dout, dq, dk, dv, delta, B, H, S, D, scale, causal,
+                          kDefaultWaitTimeoutNs, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,703 @@
+// attn_bwd_sm103.cu — gradient of the fused attention forward on GB300 (sm_103a).
+//
+// The forward is out = softmax(scale·q·kᵀ + causal mask)·v, as defined step by
+// step in "Profiling in PyTorch (Part 3): Attention is all you profile",
+// section "Naive attention"; the same page's passage on in-place operations
+// notes that the backward reuses what the forward saved.  Here the forward
+// saved out and the row logsumexp lse, so the weights are recomputed tile by
+// tile, P = exp(scale·q·kᵀ − lse), and the chain rule through the five steps
+// gives, with dP = dout·vᵀ and delta_i = rowsum(dout ⊙ out)_i:
+//
+//   dS = P ⊙ (dP − delta),   dq = scale·dS·k,   dk = scale·dSᵀ·q,   dv = Pᵀ·dout.
+//
+// As in the forward (FlashAttention-2 blog, "FlashAttention-2 Optimizations")
+// no [S, S] matrix reaches HBM and tiles above the causal diagonal are skipped.
+// Two kernels, each owning the rows it writes, so no gradient is accumulated
+// with atomics and the result does not depend on scheduling:
+//
+//   attn_bwd_dq_kernel    one CTA per (b·H + h, 128-row Q tile), walking the
+//                         K/V tiles: S = Q·Kᵀ, dP = dO·Vᵀ, dS, dQ += dS·K.
+//                         It also computes delta for its rows and stores it.
+//   attn_bwd_dkdv_kernel  one CTA per (b·H + h, 128-row K/V tile), walking the
+//                         Q tiles: Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ, Pᵀ and dSᵀ,
+//                         dV += Pᵀ·dO, dK += dSᵀ·Q.
+//
+// GB300 mapping (per CTA): warps 0-7 do the elementwise work, one thread per
+// TMEM lane (a tile row), warps 0-3 on columns 0-63 and warps 4-7 on columns
+// 64-127; warp 8 issues tcgen05.mma (operands from shared memory via TMA,
+// 128-byte swizzle; the P / dS operands straight from TMEM); warp 9 feeds the
+// shared-memory rings with TMA.  Accumulators live in TMEM:
+//   dq kernel:    S [0,128), dP [128,256), dQ [256,256+D)
+//   dk/dv kernel: Sᵀ [0,128), dPᵀ [128,256), dV [256,256+D), dK [256+D,256+2D)
+// A group stores its bf16 results (two per 32-bit column) over the first 32
+// of the 64 columns it has just read, so the A operand of the next MMA sits in
+// columns [0,32) ∪ [64,96) of its region.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn_bwd.h"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace ea {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kDrainLimitNs = 1000000000ull;  // bound on waits while tearing down
+constexpr int kTileRows = 128;
+constexpr int kChunkBytes = kTileRows * 128;  // one 64-column, 128-row swizzled block
+
+// Wait-site tags recorded in status[1] by the first wait that runs out.
+enum : int {
+  kSiteDqProducer = 0x1100, kSiteDqMmaQ = 0x1200, kSiteDqMmaKV = 0x1300, kSiteDqMmaP = 0x1400,
+  kSiteDqElemS = 0x1500, kSiteDqElemO = 0x1600,
+  kSiteKvProducer = 0x2100, kSiteKvMmaKV = 0x2200, kSiteKvMmaQ = 0x2300, kSiteKvMmaP = 0x2400,
+  kSiteKvElemS = 0x2500, kSiteKvElemO = 0x2600
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+__device__ __forceinline__ float dot_bf16x8(uint4 a, uint4 b) {
+  float s = bf16_lo(a.x) * bf16_lo(b.x);
+  s = fmaf(bf16_hi(a.x), bf16_hi(b.x), s);
+  s = fmaf(bf16_lo(a.y), bf16_lo(b.y), s);
+  s = fmaf(bf16_hi(a.y), bf16_hi(b.y), s);
+  s = fmaf(bf16_lo(a.z), bf16_lo(b.z), s);
+  s = fmaf(bf16_hi(a.z), bf16_hi(b.z), s);
+  s = fmaf(bf16_lo(a.w), bf16_lo(b.w), s);
+  s = fmaf(bf16_hi(a.w), bf16_hi(b.w), s);
+  return s;
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float2 ld_shared_f32x2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+// One warp's 32 rows × 64 columns of an fp32 TMEM accumulator, times `mul`,
+// to bf16 in the 128-byte-swizzled staging block `chunk_base` (row = TMEM
+// lane), then one TMA store of the warp's rows.  Only lane 0 issues the store.
+__device__ __forceinline__ void store_chunk(uint32_t tmem_col, uint32_t chunk_base, int row,
+                                            float mul, const CUtensorMap* map, int x, int y0,
+                                            int z, int wq, int lane) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tmem_col + half * 32, o);
+    tmem_ld_wait();
+    reg_fence(o);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int u16 = half * 4 + q4;  // 16-byte unit along the 128-byte row
+      const uint32_t addr = chunk_base + row * 128 + ((u16 ^ (row & 7)) << 4);
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * mul,
+                           __uint_as_float(o[q4 * 8 + 2 * e + 1]) * mul);
+      st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) tma_store_3d(map, chunk_base + wq * 32 * 128, x, y0 + wq * 32, z);
+}
+
+// ============================================================== dq kernel
+
+template <int D>
+struct DqLayout {
+  static constexpr int kTile = kTileRows * D * 2;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kStages = (D == 128) ? 2 : 3;  // K/V ring depth
+  static constexpr int kQOff = 0;
+  static constexpr int kDoOff = kTile;
+  static constexpr int kKOff = 2 * kTile;
+  static constexpr int kVOff = kKOff + kStages * kTile;
+  static constexpr int kPartOff = kVOff + kStages * kTile;  // float [2][128] delta halves
+  static constexpr int kBarOff = kPartOff + 2 * kTileRows * 4;
+  static constexpr int kQFull = 0;                  // Q and dO landed
+  static constexpr int kKFull = 1;                  // [kStages]
+  static constexpr int kKEmpty = kKFull + kStages;  // [kStages]
+  static constexpr int kVFull = kKEmpty + kStages;  // [kStages]
+  static constexpr int kVEmpty = kVFull + kStages;  // [kStages]
+  static constexpr int kSFull = kVEmpty + kStages;  // S and dP computed
+  static constexpr int kPFull = kSFull + 1;         // dS stored (256 arrivals)
+  static constexpr int kOFull = kPFull + 1;         // dQ final
+  static constexpr int kDrain = kOFull + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kAlloc = kMiscOff + 16 + 1024;
+  static_assert(kAlloc <= 232448, "shared memory budget exceeded");
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using L = DqLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  auto bar = [sb](int idx) -> uint32_t { return sb + L::kBarOff + 8u * idx; };
+  const uint32_t tmem_slot = sb + L::kMiscOff;
+  const uint32_t abort_addr = sb + L::kMiscOff + 4;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Q tile i of slice bh; the tiles with the most K/V tiles first
+  const int level = blockIdx.x / p.BH;
+  const int bh = blockIdx.x - level * p.BH;
+  const int i = p.n_t - 1 - level;
+  const int nkv = CAUSAL ? i + 1 : p.n_t;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kQFull), 1);
+#pragma unroll
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar(L::kKFull + s), 1);
+      mbar_init(bar(L::kKEmpty + s), 1);
+      mbar_init(bar(L::kVFull + s), 1);
+      mbar_init(bar(L::kVEmpty + s), 1);
+    }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kPFull), 256);
+    mbar_init(bar(L::kOFull), 1);
+    mbar_init(bar(L::kDrain), 1);
+    st_volatile_shared(abort_addr, 0);
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = static_cast<uint32_t>(ld_volatile_shared(tmem_slot));
+  const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
+
+  if (warp < 8) {
+    // ======================= elementwise: delta, dS, epilogue =======================
+    const int g = warp >> 2;   // column half of every tile
+    const int wq = warp & 3;   // TMEM lane quarter
+    const int row = wq * 32 + lane;
+    const int grow = i * kTileRows + row;
+    const bool valid = grow < p.S;
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem_base + lane_bits + 64 * g;
+    const uint32_t tP = tmem_base + lane_bits + 128 + 64 * g;
+    const uint32_t tQ = tmem_base + lane_bits + 256;
+
+    // delta = rowsum(dout ⊙ out): each group sums half of the row
+    float part = 0.f;
+    if (valid) {
+      const int64_t base = ((int64_t)bh * p.S + grow) * D;
+      const uint4* o4 = reinterpret_cast<const uint4*>(p.out + base) + g * (D / 16);
+      const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + base) + g * (D / 16);
+#pragma unroll
+      for (int u = 0; u < D / 16; ++u) part += dot_bf16x8(__ldg(o4 + u), __ldg(d4 + u));
+    }
+    st_shared_f32(sb + L::kPartOff + 4 * (g * kTileRows + row), part);
+    named_bar_sync(1, 256);
+    const float delta = ld_shared_f32(sb + L::kPartOff + 4 * row) +
+                        ld_shared_f32(sb + L::kPartOff + 4 * (kTileRows + row));
+    if (g == 0 && valid) p.delta[(int64_t)bh * p.S + grow] = delta;
+    const float lse2 = valid ? p.lse[(int64_t)bh * p.S + grow] * kLog2e : 0.f;
+    const float sl2 = p.scale_log2;
+
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kSFull), j & 1, ctl, kSiteDqElemS | (j & 0xff)));
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t s[2][32], dp[2][32];
+      tmem_ld_32x32b_x32(tS, s[0]);
+      tmem_ld_32x32b_x32(tS + 32, s[1]);
+      tmem_ld_32x32b_x32(tP, dp[0]);
+      tmem_ld_32x32b_x32(tP + 32, dp[1]);
+      tmem_ld_wait();
+      reg_fence(s[0]);
+      reg_fence(s[1]);
+      reg_fence(dp[0]);
+      reg_fence(dp[1]);
+      // allowed key columns of this group: 0 .. lim (causal: key <= query; key < S)
+      const int c0 = j * kTileRows + 64 * g;
+      int lim = p.S - 1 - c0;
+      if (CAUSAL) lim = min(lim, grow - c0);
+      if (!valid) lim = -1;
+      const bool edge = lim < 63;
+      uint32_t pk[32];
+#pragma unroll
+      for (int e2 = 0; e2 < 32; ++e2) {
+        const int h = e2 >> 4;
+        const int e = (2 * e2) & 31;
+        float p0 = ex2_approx(fmaf(__uint_as_float(s[h][e]), sl2, -lse2));
+        float p1 = ex2_approx(fmaf(__uint_as_float(s[h][e + 1]), sl2, -lse2));
+        if (edge) {
+          if (2 * e2 > lim) p0 = 0.f;
+          if (2 * e2 + 1 > lim) p1 = 0.f;
+        }
+        const float ds0 = p0 * (__uint_as_float(dp[h][e]) - delta);
+        const float ds1 = p1 * (__uint_as_float(dp[h][e + 1]) - delta);
+        pk[e2] = pack_bf16x2(ds0, ds1);
+      }
+      tmem_st_32x32b_x32(tS, pk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kPFull));
+    }
+
+    // ---- epilogue: dQ · scale → bf16 → swizzled staging (Q's buffer) → TMA store
+    if (ok) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kOFull), 0, ctl, kSiteDqElemO));
+    }
+    if (ok) {
+      tc_fence_after_sync();
+      for (int c = g; c < L::kChunks; c += 2)
+        store_chunk(tQ + c * 64, sb + L::kQOff + c * kChunkBytes, row, p.scale, &p.tm_dq, c * 64,
+                    i * kTileRows, bh, wq, lane);
+      if (lane == 0) {
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    }
+    tc_fence_before_sync();
+  } else if (warp == 9) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_dq);
+      const uint64_t pol_once = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      mbar_arrive_expect_tx(bar(L::kQFull), 2 * L::kTile);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(sb + L::kQOff + c * kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64,
+                    i * kTileRows, bh, pol_once);
+        tma_load_3d(sb + L::kDoOff + c * kChunkBytes, &p.tm_do, bar(L::kQFull), c * 64,
+                    i * kTileRows, bh, pol_once);
+      }
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % L::kStages;
+        const uint32_t par = ((j / L::kStages) & 1) ^ 1;
+        ok = wait_bounded(bar(L::kKEmpty + s), par, ctl, kSiteDqProducer | (j & 0xff));
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTile);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sb + L::kKOff + s * L::kTile + c * kChunkBytes, &p.tm_k, bar(L::kKFull + s),
+                      c * 64, j * kTileRows, bh, pol_kv);
+        k_issued = j + 1;
+        ok = wait_bounded(bar(L::kVEmpty + s), par, ctl, kSiteDqProducer | 0x80 | (j & 0x7f));
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTile);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sb + L::kVOff + s * L::kTile + c * kChunkBytes, &p.tm_v, bar(L::kVFull + s),
+                      c * 64, j * kTileRows, bh, pol_kv);
+        v_issued = j + 1;
+      }
+      if (ok) {
+        // every stage released by the tensor core before this CTA may exit
+        for (int j = max(nkv - L::kStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(bar(L::kKEmpty + j % L::kStages), (j / L::kStages) & 1, ctl,
+                            kSiteDqProducer | 0xff);
+        for (int j = max(nkv - L::kStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(bar(L::kVEmpty + j % L::kStages), (j / L::kStages) & 1, ctl,
+                            kSiteDqProducer | 0xfe);
+      }
+      if (!ok) {
+        wait_drain(bar(L::kQFull), 0, kDrainLimitNs);
+        for (int j = max(k_issued - L::kStages, 0); j < k_issued; ++j)
+          wait_drain(bar(L::kKFull + j % L::kStages), (j / L::kStages) & 1, kDrainLimitNs);
+        for (int j = max(v_issued - L::kStages, 0); j < v_issued; ++j)
+          wait_drain(bar(L::kVFull + j % L::kStages), (j / L::kStages) & 1, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ======================= tcgen05 issuer (warp 8) =======================
+    const bool leader = elect_one();
+    constexpr uint32_t kIdescS = instr_desc_bf16(kTileRows, kTileRows, false, false);
+    constexpr uint32_t kIdescQ = instr_desc_bf16(kTileRows, D, false, true);
+    constexpr uint32_t kTileUnits = L::kTile >> 4;
+    const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
+    const uint64_t ddo = smem_desc_sw128(sb + L::kDoOff, 16, 1024);
+    const uint64_t dk = smem_desc_sw128(sb + L::kKOff, 16, 1024);
+    const uint64_t dv = smem_desc_sw128(sb + L::kVOff, 16, 1024);
+    const uint64_t dk_mn = smem_desc_sw128(sb + L::kKOff, kChunkBytes, 1024);
+    auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
+      return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
+    };
+    bool ok = wait_warp(bar(L::kQFull), 0, kSiteDqMmaQ);
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int s = j % L::kStages;
+      const uint32_t par = (j / L::kStages) & 1;
+      ok = wait_warp(bar(L::kKFull + s), par, kSiteDqMmaKV | (j & 0xff));
+      if (ok) ok = wait_warp(bar(L::kVFull + s), par, kSiteDqMmaKV | 0x80 | (j & 0x7f));
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // S = Q · K_jᵀ
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem_base, dq + off, dk + s * kTileUnits + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO · V_jᵀ
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem_base + 128, ddo + off, dv + s * kTileUnits + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kSFull));
+        mma_commit(bar(L::kVEmpty + s));
+      }
+      __syncwarp();
+      ok = wait_warp(bar(L::kPFull), j & 1, kSiteDqMmaP | (j & 0xff));
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)  // dQ += dS · K_j (16 key rows per step)
+          mma_ts(tmem_base + 256, tmem_base + 64 * (kk >> 2) + (kk & 3) * 8,
+                 dk_mn + s * kTileUnits + kk * (2048 >> 4), kIdescQ, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(L::kKEmpty + s));
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      if (ok) mma_commit(bar(L::kOFull));
+      mma_commit(bar(L::kDrain));
+      wait_drain(bar(L::kDrain), 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+// ============================================================== dk/dv kernel
+
+template <int D>
+struct KvLayout {
+  static constexpr int kTile = kTileRows * D * 2;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kStages = (D == 128) ? 2 : 3;  // Q/dO ring depth
+  static constexpr int kStatBytes = 2 * kTileRows * 4;  // lse·log2e [128], delta [128]
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTile;
+  static constexpr int kQOff = 2 * kTile;
+  static constexpr int kDoOff = kQOff + kStages * kTile;
+  static constexpr int kStatOff = kDoOff + kStages * kTile;
+  static constexpr int kBarOff = kStatOff + kStages * kStatBytes;
+  static constexpr int kKVFull = 0;                 // K_j and V_j landed
+  static constexpr int kFull = 1;                   // [kStages] Q_i, dO_i, stats landed
+  static constexpr int kEmpty = kFull + kStages;    // [kStages]
+  static constexpr int kSFull = kEmpty + kStages;   // Sᵀ and dPᵀ computed
+  static constexpr int kPFull = kSFull + 1;         // Pᵀ and dSᵀ stored (256 arrivals)
+  static constexpr int kOFull = kPFull + 1;         // dK, dV final
+  static constexpr int kDrain = kOFull + 1;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kAlloc = kMiscOff + 16 + 1024;
+  static_assert(kAlloc <= 232448, "shared memory budget exceeded");
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(256 + 2 * D <= 512, "TMEM budget exceeded");
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using L = KvLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  auto bar = [sb](int idx) -> uint32_t { return sb + L::kBarOff + 8u * idx; };
+  const uint32_t tmem_slot = sb + L::kMiscOff;
+  const uint32_t abort_addr = sb + L::kMiscOff + 4;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // K/V tile j of slice bh; under the mask tile j meets Q tiles j .. n_t-1,
+  // so ascending j is heaviest first
+  const int j = blockIdx.x / p.BH;
+  const int bh = blockIdx.x - j * p.BH;
+  const int i0 = CAUSAL ? j : 0;
+  const int nq = p.n_t - i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kKVFull), 1);
+#pragma unroll
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar(L::kFull + s), 1);
+      mbar_init(bar(L::kEmpty + s), 1);
+    }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kPFull), 256);
+    mbar_init(bar(L::kOFull), 1);
+    mbar_init(bar(L::kDrain), 1);
+    st_volatile_shared(abort_addr, 0);
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = static_cast<uint32_t>(ld_volatile_shared(tmem_slot));
+  const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
+
+  if (warp < 8) {
+    // ======================= elementwise: Pᵀ, dSᵀ, epilogue =======================
+    const int g = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;       // key row within the tile (TMEM lane)
+    const int gk = j * kTileRows + r;   // key row in the sequence
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem_base + lane_bits + 64 * g;
+    const uint32_t tP = tmem_base + lane_bits + 128 + 64 * g;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < nq; ++it) {
+      const int i = i0 + it;
+      const int st = it % L::kStages;
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kSFull), it & 1, ctl, kSiteKvElemS | (it & 0xff)));
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t s[2][32], dp[2][32];
+      tmem_ld_32x32b_x32(tS, s[0]);
+      tmem_ld_32x32b_x32(tS + 32, s[1]);
+      tmem_ld_32x32b_x32(tP, dp[0]);
+      tmem_ld_32x32b_x32(tP + 32, dp[1]);
+      tmem_ld_wait();
+      reg_fence(s[0]);
+      reg_fence(s[1]);
+      reg_fence(dp[0]);
+      reg_fence(dp[1]);
+      // allowed query columns of this group: lo .. hi (causal: query >= key; query < S)
+      const int c0 = i * kTileRows + 64 * g;
+      const int hi = p.S - 1 - c0;
+      int lo = CAUSAL ? gk - c0 : 0;
+      if (gk >= p.S) lo = 64;  // key row past the end: nothing
+      const bool edge = lo > 0 || hi < 63;
+      const uint32_t stat = sb + L::kStatOff + st * L::kStatBytes + 4 * 64 * g;
+      uint32_t ppk[32], dpk[32];
+#pragma unroll
+      for (int e2 = 0; e2 < 32; ++e2) {
+        const int h = e2 >> 4;
+        const int e = (2 * e2) & 31;
+        const float2 l2 = ld_shared_f32x2(stat + 8 * e2);                        // lse·log2e
+        const float2 dl = ld_shared_f32x2(stat + kTileRows * 4 + 8 * e2);        // delta
+        float p0 = ex2_approx(fmaf(__uint_as_float(s[h][e]), sl2, -l2.x));
+        float p1 = ex2_approx(fmaf(__uint_as_float(s[h][e + 1]), sl2, -l2.y));
+        if (edge) {
+          if (2 * e2 < lo || 2 * e2 > hi) p0 = 0.f;
+          if (2 * e2 + 1 < lo || 2 * e2 + 1 > hi) p1 = 0.f;
+        }
+        const float ds0 = p0 * (__uint_as_float(dp[h][e]) - dl.x);
+        const float ds1 = p1 * (__uint_as_float(dp[h][e + 1]) - dl.y);
+        ppk[e2] = pack_bf16x2(p0, p1);
+        dpk[e2] = pack_bf16x2(ds0, ds1);
+      }
+      tmem_st_32x32b_x32(tS, ppk);
+      tmem_st_32x32b_x32(tP, dpk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kPFull));
+    }
+
+    // ---- epilogue: group 0 stores dV (staged in V_j's buffer), group 1 dK · scale
+    if (ok) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kOFull), 0, ctl, kSiteKvElemO));
+    }
+    if (ok) {
+      tc_fence_after_sync();
+      const uint32_t tAcc = tmem_base + lane_bits + 256 + g * D;
+      const uint32_t stage = sb + (g == 0 ? L::kVOff : L::kKOff);
+      const CUtensorMap* map = g == 0 ? &p.tm_dv : &p.tm_dk;
+      const float mul = g == 0 ? 1.f : p.scale;
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        store_chunk(tAcc + c * 64, stage + c * kChunkBytes, r, mul, map, c * 64, j * kTileRows, bh,
+                    wq, lane);
+      if (lane == 0) {
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    }
+    tc_fence_before_sync();
+  } else if (warp == 9) {
+    // ======================= producer: K_j, V_j once; Q_i, dO_i, stats per step =======================
+    const uint64_t pol_once = l2_policy_evict_first();
+    const uint64_t pol_q = l2_policy_evict_last();
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_dk);
+      tma_prefetch_desc(&p.tm_dv);
+      mbar_arrive_expect_tx(bar(L::kKVFull), 2 * L::kTile);
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(sb + L::kKOff + c * kChunkBytes, &p.tm_k, bar(L::kKVFull), c * 64,
+                    j * kTileRows, bh, pol_once);
+        tma_load_3d(sb + L::kVOff + c * kChunkBytes, &p.tm_v, bar(L::kKVFull), c * 64,
+                    j * kTileRows, bh, pol_once);
+      }
+    }
+    const int64_t row0 = (int64_t)bh * p.S;
+    int issued = 0;
+    bool ok = true;
+    for (int it = 0; it < nq; ++it) {
+      const int i = i0 + it;
+      const int st = it % L::kStages;
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kEmpty + st), ((it / L::kStages) & 1) ^ 1,
+                                                ctl, kSiteKvProducer | (it & 0xff)));
+      if (!ok) break;
+      // per-query-row statistics of Q tile i; rows past the end read as 0
+      const uint32_t stat = sb + L::kStatOff + st * L::kStatBytes;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int c = lane + 32 * t;
+        const int q = i * kTileRows + c;
+        const bool in = q < p.S;
+        st_shared_f32(stat + 4 * c, in ? p.lse[row0 + q] * kLog2e : 0.f);
+        st_shared_f32(stat + kTileRows * 4 + 4 * c, in ? p.delta[row0 + q] : 0.f);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(L::kFull + st), 2 * L::kTile);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_3d(sb + L::kQOff + st * L::kTile + c * kChunkBytes, &p.tm_q, bar(L::kFull + st),
+                      c * 64, i * kTileRows, bh, pol_q);
+          tma_load_3d(sb + L::kDoOff + st * L::kTile + c * kChunkBytes, &p.tm_do,
+                      bar(L::kFull + st), c * 64, i * kTileRows, bh, pol_q);
+        }
+      }
+      issued = it + 1;
+      __syncwarp();
+    }
+    if (lane == 0) {
+      if (ok) {
+        for (int it = max(nq - L::kStages, 0); it < nq && ok; ++it)
+          ok = wait_bounded(bar(L::kEmpty + it % L::kStages), (it / L::kStages) & 1, ctl,
+                            kSiteKvProducer | 0xff);
+      }
+      if (!ok) {
+        wait_drain(bar(L::kKVFull), 0, kDrainLimitNs);
+        for (int it = max(issued - L::kStages, 0); it < issued; ++it)
+          wait_drain(bar(L::kFull + it % L::kStages), (it / L::kStages) & 1, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ======================= tcgen05 issuer (warp 8) =======================
+    const bool leader = elect_one();
+    constexpr uint32_t kIdescS = instr_desc_bf16(kTileRows, kTileRows, false, false);
+    constexpr uint32_t kIdescG = instr_desc_bf16(kTileRows, D, false, true);
+    constexpr uint32_t kTileUnits = L::kTile >> 4;
+    const uint64_t dk = smem_desc_sw128(sb + L::kKOff, 16, 1024);
+    const uint64_t dv = smem_desc_sw128(sb + L::kVOff, 16, 1024);
+    const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
+    const uint64_t ddo = smem_desc_sw128(sb + L::kDoOff, 16, 1024);
+    const uint64_t dq_mn = smem_desc_sw128(sb + L::kQOff, kChunkBytes, 1024);
+    const uint64_t ddo_mn = smem_desc_sw128(sb + L::kDoOff, kChunkBytes, 1024);
+    auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
+      return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
+    };
+    bool ok = wait_warp(bar(L::kKVFull), 0, kSiteKvMmaKV);
+    for (int it = 0; it < nq && ok; ++it) {
+      const int st = it % L::kStages;
+      ok = wait_warp(bar(L::kFull + st), (it / L::kStages) & 1, kSiteKvMmaQ | (it & 0xff));
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // Sᵀ = K_j · Q_iᵀ
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem_base, dk + off, dq + st * kTileUnits + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // dPᵀ = V_j · dO_iᵀ
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem_base + 128, dv + off, ddo + st * kTileUnits + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kSFull));
+      }
+      __syncwarp();
+      ok = wait_warp(bar(L::kPFull), it & 1, kSiteKvMmaP | (it & 0xff));
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk) {  // 16 query rows per step
+          const uint32_t a = 64 * (kk >> 2) + (kk & 3) * 8;
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          mma_ts(tmem_base + 256, tmem_base + a, ddo_mn + st * kTileUnits + kk * (2048 >> 4),
+                 kIdescG, acc);  // dV += Pᵀ · dO_i
+          mma_ts(tmem_base + 256 + D, tmem_base + 128 + a, dq_mn + st * kTileUnits + kk * (2048 >> 4),
+                 kIdescG, acc);  // dK += dSᵀ · Q_i
+        }
+        mma_commit(bar(L::kEmpty + st));
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      if (ok) mma_commit(bar(L::kOFull));
+      mma_commit(bar(L::kDrain));
+      wait_drain(bar(L::kDrain), 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream) {
+  auto kdq = attn_bwd_dq_kernel<D, CAUSAL>;
+  auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DqLayout<D>::kAlloc);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvLayout<D>::kAlloc);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>((long long)p.BH * p.n_t);
+  kdq<<<grid, kBwdThreads, DqLayout<D>::kAlloc, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  kkv<<<grid, kBwdThreads, KvLayout<D>::kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t bwd_launch(const BwdParams& p, int D, bool causal, cudaStream_t stream) {
+  if (D == 64) return causal ? launch_impl<64, true>(p, stream) : launch_impl<64, false>(p, stream);
+  return causal ? launch_impl<128, true>(p, stream) : launch_impl<128, false>(p, stream);
+}
+
+}  // namespace ea

@@ -22,4 +22,8 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
                                  float scale, int causal, uint64_t timeout_ns, int* status,
                                  cudaStream_t stream);
 
+// The current device's status word pair (allocated on first use), after the
+// architecture check.
+attn_status_t current_status_words(int** status);
+
 }  // namespace ea

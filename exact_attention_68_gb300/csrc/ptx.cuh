@@ -102,7 +102,7 @@ constexpr uint32_t kSuspendHintNs = 200000;
 // Device status bits (combined with atomicOr in the global status word).
 enum : int { kStatusTimeout = 1 };
 
-__device__ __noinline__ void raise_abort(const WaitCtl& c, int where) {
+static __device__ __noinline__ void raise_abort(const WaitCtl& c, int where) {
   st_volatile_shared(c.abort_flag, 1);
   if (c.status != nullptr) {
     atomicOr(c.status, kStatusTimeout);

@@ -1,5 +1,6 @@
 /*
- * attn.h — C ABI of the GB300 (sm_103a) fused exact attention forward.
+ * attn.h — C ABI of the GB300 (sm_103a) fused exact attention forward and
+ * its gradient (attn_bwd, near the end).
  *
  * The operation (what every entry point below computes) is the one spelled
  * out step by step in "Profiling in PyTorch (Part 3): Attention is all you
@@ -152,6 +153,47 @@ ATTN_API attn_status_t attn_fwd_noalloc(const void* q, const void* k, const void
                                         float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
                                         float scale, int causal, int check_status,
                                         cudaStream_t stream);
+
+/*
+ * attn_bwd — gradient of attn_fwd with respect to q, k and v.
+ *
+ * The pages define the forward only; the same profiling page's passage on
+ * in-place operations notes that the backward reuses what the forward saved.
+ * For an upstream gradient dout = ∂L/∂out this computes the exact gradient of
+ * the five forward steps (chain rule in reverse): with P the attention weights
+ * recomputed from the saved lse, dP = dout·vᵀ and
+ * delta_i = Σ_d dout[i,d]·out[i,d],
+ *
+ *     dS = P ⊙ (dP − delta),  dq = scale·dS·k,  dk = scale·dSᵀ·q,  dv = Pᵀ·dout.
+ *
+ *   q, k, v     the forward's inputs, device bf16 [B, H, S, D], 16-byte aligned (read)
+ *   out, lse    the forward's results for those inputs: out bf16 [B, H, S, D]
+ *               (16-byte aligned), lse fp32 [B, H, S] (4-byte aligned) (read)
+ *   dout        device bf16 [B, H, S, D], 16-byte aligned (read)
+ *   dq, dk, dv  device bf16 [B, H, S, D], 16-byte aligned (written)
+ *   delta       device fp32 [B, H, S], 4-byte aligned: workspace the call
+ *               writes (rowsum(dout ⊙ out)) and reads back; its contents after
+ *               the call are that rowsum
+ *   B, H, S, D, scale, causal, stream   as for attn_fwd (the same values the
+ *               forward used)
+ *
+ * Two kernels are enqueued on `stream` (dq and delta, then dk and dv); each
+ * gradient row is written by exactly one CTA, with no atomics, so results are
+ * bitwise reproducible.  Asynchronous; allocates nothing beyond the status
+ * word attn_fwd also uses.  Outputs must not overlap each other or any input.
+ * Errors as attn_fwd; a wait that runs out is reported by attn_device_status.
+ */
+ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                float* delta, int64_t B, int64_t H, int64_t S, int64_t D,
+                                float scale, int causal, cudaStream_t stream);
+
+/* attn_bwd with an explicit bound on every in-kernel wait (see attn_fwd_bounded). */
+ATTN_API attn_status_t attn_bwd_bounded(const void* q, const void* k, const void* v,
+                                        const void* out, const float* lse, const void* dout,
+                                        void* dq, void* dk, void* dv, float* delta, int64_t B,
+                                        int64_t H, int64_t S, int64_t D, float scale, int causal,
+                                        uint64_t wait_timeout_ns, cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status_t status);

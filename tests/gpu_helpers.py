@@ -37,3 +37,65 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
     assert summary["out_mean"] <= OUT_MEAN_TOL, (what, summary)
     assert summary["lse_max"] <= LSE_TOL, (what, summary)
     return summary
+
+
+# ---------------------------------------------------------------- backward
+# Element-wise bar for the gradients.  The kernel rounds P and dS to bf16
+# (unit roundoff 2^-8) before the tensor core multiplies them by exact bf16
+# operands with fp32 accumulation, computes delta_i from the bf16 `out`
+# (error <= 2^-8 · E_i, E_i = Σ_d |dout_id · out_id|) and rounds each gradient
+# to bf16.  So each element obeys |err| <= 2^-8 · (M + |ref|) up to fp32
+# terms, with M the magnitude sum of what it accumulates:
+#   dv_j: Σ_i attn_ij |dout_i|
+#   dk_j: scale · Σ_i (|dz_ij| + attn_ij E_i) |q_i|
+#   dq_i: scale · Σ_j (|dz_ij| + attn_ij E_i) |k_j|
+# The tests allow twice that, 2^-7, plus 1e-6 absolute.
+BWD_REL = 2.0 ** -7
+BWD_ABS = 1e-6
+
+
+def bwd_magnitudes(q, k, v, dout, scale, causal, b, h, q_rows, kv_rows, chunk=1024):
+    """M_q[q_rows], M_k[kv_rows], M_v[kv_rows] of one (b, h), float64 numpy."""
+    qh, kh, vh, dh = (np.asarray(x[b, h], dtype=np.float64) for x in (q, k, v, dout))
+    S = qh.shape[0]
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    kv_rows = np.asarray(kv_rows, dtype=np.int64)
+    Mq = np.zeros((q_rows.size, qh.shape[1]))
+    Mk = np.zeros((kv_rows.size, qh.shape[1]))
+    Mv = np.zeros((kv_rows.size, qh.shape[1]))
+    want_q = {int(r): n for n, r in enumerate(q_rows)}
+    for r0 in range(0, S, chunk):
+        rows = np.arange(r0, min(S, r0 + chunk))
+        s = (qh[rows] @ kh.T) * scale
+        if causal:
+            s = np.where(np.arange(S)[None, :] > rows[:, None], -np.inf, s)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        attn = e / e.sum(axis=1, keepdims=True)
+        out = attn @ vh
+        dattn = dh[rows] @ vh.T
+        delta = np.sum(dh[rows] * out, axis=1, keepdims=True)
+        dz = np.abs(attn * (dattn - delta))
+        E = np.sum(np.abs(dh[rows] * out), axis=1, keepdims=True)
+        w = dz + attn * E                       # [rows, S]
+        Mk += scale * (w[:, kv_rows].T @ np.abs(qh[rows]))
+        Mv += attn[:, kv_rows].T @ np.abs(dh[rows])
+        for n_local, r in enumerate(rows):
+            if int(r) in want_q:
+                Mq[want_q[int(r)]] = scale * (w[n_local] @ np.abs(kh))
+    return Mq, Mk, Mv
+
+
+def compare_grad(got, ref, mag, what=""):
+    """Element-wise |got - ref| <= BWD_REL·(mag + |ref|) + BWD_ABS; returns a summary."""
+    got = np.asarray(got, np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite gradient"
+    err = np.abs(got - ref)
+    bound = BWD_REL * (mag + np.abs(ref)) + BWD_ABS
+    worst = float((err / bound).max()) if err.size else 0.0
+    rel_fro = float(np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30))
+    summary = dict(worst_ratio=worst, max_err=float(err.max()) if err.size else 0.0,
+                   rel_fro=rel_fro)
+    assert worst <= 1.0, (what, summary)
+    assert rel_fro <= BWD_REL, (what, summary)
+    return summary

@@ -106,3 +106,42 @@ def test_noalloc_validates_before_touching_the_gpu(lib):
     bad = list(args)
     bad[8] = 80
     assert lib.attn_fwd_noalloc(*bad, 1, None) == binding.ATTN_ERR_UNSUPPORTED
+
+
+def _bwd(lib, q=A, k=A + T, v=A + 2 * T, out=A + 3 * T, lse=A + 4 * T, dout=A + 5 * T,
+         dq=A + 6 * T, dk=A + 7 * T, dv=A + 8 * T, delta=A + 9 * T,
+         B=1, H=2, S=128, D=64, scale=0.125, causal=1):
+    return lib.attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, delta, B, H, S, D, scale, causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(out=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(dout=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(dq=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(dk=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(dv=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(delta=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(S=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(causal=3), binding.ATTN_ERR_INVALID_ARG),
+    (dict(dout=A + 5 * T + 8), binding.ATTN_ERR_MISALIGNED),
+    (dict(dq=A + 6 * T + 4), binding.ATTN_ERR_MISALIGNED),
+    (dict(dv=A + 8 * T + 2), binding.ATTN_ERR_MISALIGNED),
+    (dict(delta=A + 9 * T + 2), binding.ATTN_ERR_MISALIGNED),
+    (dict(dq=A), binding.ATTN_ERR_INVALID_ARG),               # dq aliases q
+    (dict(dk=A + 5 * T), binding.ATTN_ERR_INVALID_ARG),       # dk aliases dout
+    (dict(dv=A + 6 * T + 64), binding.ATTN_ERR_INVALID_ARG),  # dv inside dq
+    (dict(delta=A + 4 * T), binding.ATTN_ERR_INVALID_ARG),    # delta aliases lse
+    (dict(delta=A + 8 * T + 128), binding.ATTN_ERR_INVALID_ARG),  # delta inside dv
+])
+def test_bwd_invalid_arguments_are_rejected_before_launch(lib, kw, code):
+    assert _bwd(lib, **kw) == code
+
+
+def test_bwd_bounded_validates_too(lib):
+    args = [A, A + T, A + 2 * T, A + 3 * T, A + 4 * T, 0, A + 6 * T, A + 7 * T, A + 8 * T,
+            A + 9 * T, 1, 2, 128, 64, 0.125, 1]
+    assert lib.attn_bwd_bounded(*args, 0, None) == binding.ATTN_ERR_INVALID_ARG

@@ -53,3 +53,22 @@ def test_argument_errors_on_gpu_launch_nothing(cuda_device):
     assert rc == binding.ATTN_ERR_MISALIGNED
     torch.cuda.synchronize()
     assert (out == 7.0).all() and (lse == 7.0).all()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_bwd_forced_wait_timeout_reports_and_recovers(cuda_device, D):
+    shape = (2, 2, 1024, D)
+    q, k, v = (x.to("cuda:0") for x in make_qkv(shape, seed=23))
+    out, lse = binding.attn_fwd(q, k, v, causal=True)
+    dout = torch.ones_like(q)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.ATTN_OK
+    binding.attn_bwd_bounded(q, k, v, out, lse, dout, causal=True, wait_timeout_ns=0)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.ATTN_ERR_TIMEOUT
+    assert binding.device_status() == binding.ATTN_OK
+    # the next normal call runs to completion
+    dq, dk, dv, _ = binding.attn_bwd(q, k, v, out, lse, dout, causal=True)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.ATTN_OK
+    assert all(torch.isfinite(t.float()).all() for t in (dq, dk, dv))
