@@ -275,6 +275,31 @@ def side_workloads(device, stream):
     return res
 
 
+def backward_leg(w, q, k, v, out, lse, scale, stream, steps):
+    """The gradient of the same workload (attn_bwd: dq+delta kernel, then dk/dv
+    kernel), timed over `steps` calls with CUDA events after 3 warm-up calls."""
+    from exact_attention_68_gb300 import binding
+    g = torch.Generator().manual_seed(1)
+    dout = torch.randn(w.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(q.device)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    delta = torch.empty_like(lse)
+
+    def call():
+        binding.attn_bwd(q, k, v, out, lse, dout, scale, w.causal, dq, dk, dv, delta)
+
+    for _ in range(3):
+        call()
+    ms = time_steps(call, steps, stream) / steps
+    counted = 2.5 * counted_flops(w.B, w.H, w.S, w.D, w.causal)
+    executed = 3.5 * executed_flops(w.B, w.H, w.S, w.D, w.causal)
+    return {"metric": "attention backward TFLOP/s (counted: 2.5x the forward's FLOPs)",
+            "value": counted / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "steps": steps, "executed_tflops": executed / (ms * 1e-3) / 1e12,
+            "executed_over_counted_flops": executed / counted,
+            "kernels": ["attn_bwd_dq_kernel<128,true>", "attn_bwd_dkdv_kernel<128,true>"],
+            "gpu_launches": 2 * steps}
+
+
 def run_ours(args, world, rank, local):
     from exact_attention_68_gb300 import binding
     from exact_attention_68_gb300.build import build_library
@@ -344,6 +369,12 @@ def run_ours(args, world, rank, local):
     extra = {}
     if rank == 0 and world == 1 and not args.no_side:
         extra["other_workloads"] = side_workloads(device, stream)
+    if not args.no_bwd:
+        bwd = backward_leg(w, q, k, v, out, lse, scale, stream, max(3, min(args.steps, 50)))
+        bwd["roofline"] = {"bound": "tensor", "achieved": bwd["value"],
+                           "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                           "frac": bwd["value"] / float(peaks["bf16_tflops"])}
+        extra["backward"] = bwd
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         tf, n_rows, secs = oracle_rows_sample(*as_numpy(q_h, k_h, v_h), scale, w.causal, 256,
@@ -395,6 +426,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-side", action="store_true", help="skip the other-workload timings")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward timing")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--shape", default=None,
                     help="B,H,S,D of a causal workload to time instead (profiling runs)")
