@@ -23,15 +23,23 @@
 //                         dV += Pᵀ·dO, dK += dSᵀ·Q.
 //
 // GB300 mapping (per CTA): warps 0-7 do the elementwise work, one thread per
-// TMEM lane (a tile row), warps 0-3 on columns 0-63 and warps 4-7 on columns
-// 64-127; warp 8 issues tcgen05.mma (operands from shared memory via TMA,
-// 128-byte swizzle; the P / dS operands straight from TMEM); warp 9 feeds the
-// shared-memory rings with TMA.  Accumulators live in TMEM:
-//   dq kernel:    S [0,128), dP [128,256), dQ [256,256+D)
-//   dk/dv kernel: Sᵀ [0,128), dPᵀ [128,256), dV [256,256+D), dK [256+D,256+2D)
-// A group stores its bf16 results (two per 32-bit column) over the first 32
-// of the 64 columns it has just read, so the A operand of the next MMA sits in
-// columns [0,32) ∪ [64,96) of its region.
+// TMEM lane (a tile row); warp 8 issues tcgen05.mma (operands from shared
+// memory via TMA, 128-byte swizzle; the P / dS operands straight from TMEM);
+// warp 9 feeds the shared-memory rings with TMA.  Every 128-column tile of the
+// loop is handled as two 64-column halves with a TMEM buffer each, and
+// warpgroup g (warps 4g..4g+3) always takes half g: while one warpgroup does
+// its half's elementwise work, the tensor core runs the other half's MMAs.
+// The MMA order per step t is G(t,0), SP(t+1,0), G(t,1), SP(t+1,1), where SP
+// is a half's S/dP products and G its gradient products, so each half's
+// elementwise work is covered by about 1300 cycles of tensor work.
+// TMEM columns:
+//   dq kernel:    half h: S_h [128h, 128h+64), dP_h [128h+64, 128h+128);
+//                 dQ [256, 256+D)
+//   dk/dv kernel: half h: Sᵀ_h [128h, 128h+64), dPᵀ_h [128h+64, 128h+128);
+//                 dV [256, 256+D), dK [256+D, 256+2D)
+// A warpgroup stores its bf16 results (two per 32-bit column) over the first
+// 32 columns of the S and dP blocks it has just read: they are the A operand
+// of the half's gradient MMAs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -79,10 +87,8 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ float2 ld_shared_f32x2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_shared_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
 // One warp's 32 rows × 64 columns of an fp32 TMEM accumulator, times `mul`,
@@ -120,21 +126,22 @@ template <int D>
 struct DqLayout {
   static constexpr int kTile = kTileRows * D * 2;
   static constexpr int kChunks = D / 64;
-  static constexpr int kStages = (D == 128) ? 2 : 3;  // K/V ring depth
+  static constexpr int kKStages = (D == 128) ? 3 : 4;  // K ring depth
+  static constexpr int kVStages = (D == 128) ? 2 : 3;  // V ring depth (V is released earlier)
   static constexpr int kQOff = 0;
   static constexpr int kDoOff = kTile;
   static constexpr int kKOff = 2 * kTile;
-  static constexpr int kVOff = kKOff + kStages * kTile;
-  static constexpr int kPartOff = kVOff + kStages * kTile;  // float [2][128] delta halves
+  static constexpr int kVOff = kKOff + kKStages * kTile;
+  static constexpr int kPartOff = kVOff + kVStages * kTile;  // float [2][128] delta halves
   static constexpr int kBarOff = kPartOff + 2 * kTileRows * 4;
-  static constexpr int kQFull = 0;                  // Q and dO landed
-  static constexpr int kKFull = 1;                  // [kStages]
-  static constexpr int kKEmpty = kKFull + kStages;  // [kStages]
-  static constexpr int kVFull = kKEmpty + kStages;  // [kStages]
-  static constexpr int kVEmpty = kVFull + kStages;  // [kStages]
-  static constexpr int kSFull = kVEmpty + kStages;  // S and dP computed
-  static constexpr int kPFull = kSFull + 1;         // dS stored (256 arrivals)
-  static constexpr int kOFull = kPFull + 1;         // dQ final
+  static constexpr int kQFull = 0;                   // Q and dO landed
+  static constexpr int kKFull = 1;                   // [kKStages]
+  static constexpr int kKEmpty = kKFull + kKStages;  // [kKStages]
+  static constexpr int kVFull = kKEmpty + kKStages;  // [kVStages]
+  static constexpr int kVEmpty = kVFull + kVStages;  // [kVStages]
+  static constexpr int kSFull = kVEmpty + kVStages;  // [2] S_h and dP_h computed
+  static constexpr int kPFull = kSFull + 2;          // [2] dS_h stored (128 arrivals)
+  static constexpr int kOFull = kPFull + 2;          // dQ final
   static constexpr int kDrain = kOFull + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
@@ -163,14 +170,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
 #pragma unroll
-    for (int s = 0; s < L::kStages; ++s) {
+    for (int s = 0; s < L::kKStages; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
       mbar_init(bar(L::kKEmpty + s), 1);
+    }
+#pragma unroll
+    for (int s = 0; s < L::kVStages; ++s) {
       mbar_init(bar(L::kVFull + s), 1);
       mbar_init(bar(L::kVEmpty + s), 1);
     }
-    mbar_init(bar(L::kSFull), 1);
-    mbar_init(bar(L::kPFull), 256);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(L::kSFull + h), 1);
+      mbar_init(bar(L::kPFull + h), 128);
+    }
     mbar_init(bar(L::kOFull), 1);
     mbar_init(bar(L::kDrain), 1);
     st_volatile_shared(abort_addr, 0);
@@ -188,17 +201,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
 
   if (warp < 8) {
     // ======================= elementwise: delta, dS, epilogue =======================
-    const int g = warp >> 2;   // column half of every tile
+    const int g = warp >> 2;   // half of every K/V tile this warpgroup takes
     const int wq = warp & 3;   // TMEM lane quarter
     const int row = wq * 32 + lane;
     const int grow = i * kTileRows + row;
     const bool valid = grow < p.S;
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem_base + lane_bits + 64 * g;
-    const uint32_t tP = tmem_base + lane_bits + 128 + 64 * g;
+    const uint32_t tS = tmem_base + lane_bits + 128 * g;
+    const uint32_t tP = tS + 64;
     const uint32_t tQ = tmem_base + lane_bits + 256;
 
-    // delta = rowsum(dout ⊙ out): each group sums half of the row
+    // delta = rowsum(dout ⊙ out): each warpgroup sums half of the row
     float part = 0.f;
     if (valid) {
       const int64_t base = ((int64_t)bh * p.S + grow) * D;
@@ -217,7 +230,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
 
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kSFull), j & 1, ctl, kSiteDqElemS | (j & 0xff)));
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kSFull + g), j & 1, ctl,
+                                                kSiteDqElemS | (g << 7) | (j & 0x7f)));
       if (!ok) break;
       tc_fence_after_sync();
       uint32_t s[2][32], dp[2][32];
@@ -230,7 +244,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       reg_fence(s[1]);
       reg_fence(dp[0]);
       reg_fence(dp[1]);
-      // allowed key columns of this group: 0 .. lim (causal: key <= query; key < S)
+      // allowed key columns of this half: 0 .. lim (causal: key <= query; key < S)
       const int c0 = j * kTileRows + 64 * g;
       int lim = p.S - 1 - c0;
       if (CAUSAL) lim = min(lim, grow - c0);
@@ -254,7 +268,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       tmem_st_32x32b_x32(tS, pk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(bar(L::kPFull));
+      mbar_arrive(bar(L::kPFull + g));
     }
 
     // ---- epilogue: dQ · scale → bf16 → swizzled staging (Q's buffer) → TMA store
@@ -293,48 +307,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int j = 0; j < nkv; ++j) {
-        const int s = j % L::kStages;
-        const uint32_t par = ((j / L::kStages) & 1) ^ 1;
-        ok = wait_bounded(bar(L::kKEmpty + s), par, ctl, kSiteDqProducer | (j & 0xff));
+        const int ks = j % L::kKStages;
+        ok = wait_bounded(bar(L::kKEmpty + ks), ((j / L::kKStages) & 1) ^ 1, ctl,
+                          kSiteDqProducer | (j & 0x7f));
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTile);
+        mbar_arrive_expect_tx(bar(L::kKFull + ks), L::kTile);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sb + L::kKOff + s * L::kTile + c * kChunkBytes, &p.tm_k, bar(L::kKFull + s),
+          tma_load_3d(sb + L::kKOff + ks * L::kTile + c * kChunkBytes, &p.tm_k, bar(L::kKFull + ks),
                       c * 64, j * kTileRows, bh, pol_kv);
         k_issued = j + 1;
-        ok = wait_bounded(bar(L::kVEmpty + s), par, ctl, kSiteDqProducer | 0x80 | (j & 0x7f));
+        const int vs = j % L::kVStages;
+        ok = wait_bounded(bar(L::kVEmpty + vs), ((j / L::kVStages) & 1) ^ 1, ctl,
+                          kSiteDqProducer | 0x80 | (j & 0x7f));
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTile);
+        mbar_arrive_expect_tx(bar(L::kVFull + vs), L::kTile);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sb + L::kVOff + s * L::kTile + c * kChunkBytes, &p.tm_v, bar(L::kVFull + s),
+          tma_load_3d(sb + L::kVOff + vs * L::kTile + c * kChunkBytes, &p.tm_v, bar(L::kVFull + vs),
                       c * 64, j * kTileRows, bh, pol_kv);
         v_issued = j + 1;
       }
       if (ok) {
         // every stage released by the tensor core before this CTA may exit
-        for (int j = max(nkv - L::kStages, 0); j < nkv && ok; ++j)
-          ok = wait_bounded(bar(L::kKEmpty + j % L::kStages), (j / L::kStages) & 1, ctl,
+        for (int j = max(nkv - L::kKStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(bar(L::kKEmpty + j % L::kKStages), (j / L::kKStages) & 1, ctl,
+                            kSiteDqProducer | 0x7f);
+        for (int j = max(nkv - L::kVStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(bar(L::kVEmpty + j % L::kVStages), (j / L::kVStages) & 1, ctl,
                             kSiteDqProducer | 0xff);
-        for (int j = max(nkv - L::kStages, 0); j < nkv && ok; ++j)
-          ok = wait_bounded(bar(L::kVEmpty + j % L::kStages), (j / L::kStages) & 1, ctl,
-                            kSiteDqProducer | 0xfe);
       }
       if (!ok) {
         wait_drain(bar(L::kQFull), 0, kDrainLimitNs);
-        for (int j = max(k_issued - L::kStages, 0); j < k_issued; ++j)
-          wait_drain(bar(L::kKFull + j % L::kStages), (j / L::kStages) & 1, kDrainLimitNs);
-        for (int j = max(v_issued - L::kStages, 0); j < v_issued; ++j)
-          wait_drain(bar(L::kVFull + j % L::kStages), (j / L::kStages) & 1, kDrainLimitNs);
+        for (int j = max(k_issued - L::kKStages, 0); j < k_issued; ++j)
+          wait_drain(bar(L::kKFull + j % L::kKStages), (j / L::kKStages) & 1, kDrainLimitNs);
+        for (int j = max(v_issued - L::kVStages, 0); j < v_issued; ++j)
+          wait_drain(bar(L::kVFull + j % L::kVStages), (j / L::kVStages) & 1, kDrainLimitNs);
       }
     }
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
     const bool leader = elect_one();
-    constexpr uint32_t kIdescS = instr_desc_bf16(kTileRows, kTileRows, false, false);
+    constexpr uint32_t kIdescSP = instr_desc_bf16(kTileRows, 64, false, false);  // 64 keys
     constexpr uint32_t kIdescQ = instr_desc_bf16(kTileRows, D, false, true);
     constexpr uint32_t kTileUnits = L::kTile >> 4;
+    constexpr uint32_t kHalfUnits = (64 * 128) >> 4;  // 64 rows of a 128-byte-row block
     const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
     const uint64_t ddo = smem_desc_sw128(sb + L::kDoOff, 16, 1024);
     const uint64_t dk = smem_desc_sw128(sb + L::kKOff, 16, 1024);
@@ -343,38 +360,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
       return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
     };
+    // SP(j, h): S_h = Q · K_j[64h, 64h+64)ᵀ and dP_h = dO · V_j[64h, 64h+64)ᵀ
+    auto issue_sp = [&](int ks, int vs, int h) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ss(tmem_base + 128 * h, dq + off, dk + ks * kTileUnits + h * kHalfUnits + off,
+               kIdescSP, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ss(tmem_base + 128 * h + 64, ddo + off, dv + vs * kTileUnits + h * kHalfUnits + off,
+               kIdescSP, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::kSFull + h));
+    };
+    // G(j, h): dQ += dS_h · K_j[64h, 64h+64) (16 key rows per step)
+    auto issue_g = [&](int ks, int h, bool first) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ts(tmem_base + 256, tmem_base + 128 * h + kk * 8,
+               dk_mn + ks * kTileUnits + (4 * h + kk) * (2048 >> 4), kIdescQ,
+               (first && kk == 0) ? 0u : 1u);
+    };
+    auto wait_kv = [&](int j) {
+      bool r = wait_warp(bar(L::kKFull + j % L::kKStages), (j / L::kKStages) & 1,
+                         kSiteDqMmaKV | (j & 0x7f));
+      if (r) r = wait_warp(bar(L::kVFull + j % L::kVStages), (j / L::kVStages) & 1,
+                           kSiteDqMmaKV | 0x80 | (j & 0x7f));
+      return r;
+    };
+
     bool ok = wait_warp(bar(L::kQFull), 0, kSiteDqMmaQ);
-    for (int j = 0; j < nkv && ok; ++j) {
-      const int s = j % L::kStages;
-      const uint32_t par = (j / L::kStages) & 1;
-      ok = wait_warp(bar(L::kKFull + s), par, kSiteDqMmaKV | (j & 0xff));
-      if (ok) ok = wait_warp(bar(L::kVFull + s), par, kSiteDqMmaKV | 0x80 | (j & 0x7f));
-      if (!ok) break;
+    if (ok) ok = wait_kv(0);
+    if (ok) {
       tc_fence_after_sync();
       if (leader) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S = Q · K_jᵀ
-          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem_base, dq + off, dk + s * kTileUnits + off, kIdescS, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO · V_jᵀ
-          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem_base + 128, ddo + off, dv + s * kTileUnits + off, kIdescS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kSFull));
-        mma_commit(bar(L::kVEmpty + s));
+        issue_sp(0, 0, 0);
+        issue_sp(0, 0, 1);
+        mma_commit(bar(L::kVEmpty + 0));
       }
       __syncwarp();
-      ok = wait_warp(bar(L::kPFull), j & 1, kSiteDqMmaP | (j & 0xff));
+    }
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int ks = j % L::kKStages;
+      const bool more = j + 1 < nkv;
+      const int ksn = (j + 1) % L::kKStages;
+      const int vsn = (j + 1) % L::kVStages;
+      ok = wait_warp(bar(L::kPFull + 0), j & 1, kSiteDqMmaP | (j & 0x7f));
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) issue_g(ks, 0, j == 0);
+      __syncwarp();
+      if (more) {
+        ok = wait_kv(j + 1);
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (leader) issue_sp(ksn, vsn, 0);
+        __syncwarp();
+      }
+      ok = wait_warp(bar(L::kPFull + 1), j & 1, kSiteDqMmaP | 0x80 | (j & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
       if (leader) {
-#pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk)  // dQ += dS · K_j (16 key rows per step)
-          mma_ts(tmem_base + 256, tmem_base + 64 * (kk >> 2) + (kk & 3) * 8,
-                 dk_mn + s * kTileUnits + kk * (2048 >> 4), kIdescQ, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(L::kKEmpty + s));
+        issue_g(ks, 1, false);
+        mma_commit(bar(L::kKEmpty + ks));  // K_j: last read by G(j, 1)
+        if (more) {
+          issue_sp(ksn, vsn, 1);
+          mma_commit(bar(L::kVEmpty + vsn));  // V_{j+1}: last read by SP(j+1, 1)
+        }
       }
       __syncwarp();
     }
@@ -400,7 +455,7 @@ struct KvLayout {
   static constexpr int kTile = kTileRows * D * 2;
   static constexpr int kChunks = D / 64;
   static constexpr int kStages = (D == 128) ? 2 : 3;  // Q/dO ring depth
-  static constexpr int kStatBytes = 2 * kTileRows * 4;  // lse·log2e [128], delta [128]
+  static constexpr int kStatBytes = 2 * kTileRows * 4;  // (lse·log2e, delta) per query row
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTile;
   static constexpr int kQOff = 2 * kTile;
@@ -410,9 +465,9 @@ struct KvLayout {
   static constexpr int kKVFull = 0;                 // K_j and V_j landed
   static constexpr int kFull = 1;                   // [kStages] Q_i, dO_i, stats landed
   static constexpr int kEmpty = kFull + kStages;    // [kStages]
-  static constexpr int kSFull = kEmpty + kStages;   // Sᵀ and dPᵀ computed
-  static constexpr int kPFull = kSFull + 1;         // Pᵀ and dSᵀ stored (256 arrivals)
-  static constexpr int kOFull = kPFull + 1;         // dK, dV final
+  static constexpr int kSFull = kEmpty + kStages;   // [2] Sᵀ_h and dPᵀ_h computed
+  static constexpr int kPFull = kSFull + 2;         // [2] Pᵀ_h and dSᵀ_h stored (128 arrivals)
+  static constexpr int kOFull = kPFull + 2;         // dK, dV final
   static constexpr int kDrain = kOFull + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -427,6 +482,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   using L = KvLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint8_t* smem_gen = smem_raw + (sb - smem_u32(smem_raw));  // same window, generic
   auto bar = [sb](int idx) -> uint32_t { return sb + L::kBarOff + 8u * idx; };
   const uint32_t tmem_slot = sb + L::kMiscOff;
   const uint32_t abort_addr = sb + L::kMiscOff + 4;
@@ -447,8 +503,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       mbar_init(bar(L::kFull + s), 1);
       mbar_init(bar(L::kEmpty + s), 1);
     }
-    mbar_init(bar(L::kSFull), 1);
-    mbar_init(bar(L::kPFull), 256);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(L::kSFull + h), 1);
+      mbar_init(bar(L::kPFull + h), 128);
+    }
     mbar_init(bar(L::kOFull), 1);
     mbar_init(bar(L::kDrain), 1);
     st_volatile_shared(abort_addr, 0);
@@ -466,19 +525,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
 
   if (warp < 8) {
     // ======================= elementwise: Pᵀ, dSᵀ, epilogue =======================
-    const int g = warp >> 2;
+    const int g = warp >> 2;            // half of every Q tile this warpgroup takes
     const int wq = warp & 3;
     const int r = wq * 32 + lane;       // key row within the tile (TMEM lane)
     const int gk = j * kTileRows + r;   // key row in the sequence
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem_base + lane_bits + 64 * g;
-    const uint32_t tP = tmem_base + lane_bits + 128 + 64 * g;
+    const uint32_t tS = tmem_base + lane_bits + 128 * g;
+    const uint32_t tP = tS + 64;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int it = 0; it < nq; ++it) {
       const int i = i0 + it;
       const int st = it % L::kStages;
-      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kSFull), it & 1, ctl, kSiteKvElemS | (it & 0xff)));
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kSFull + g), it & 1, ctl,
+                                                kSiteKvElemS | (g << 7) | (it & 0x7f)));
       if (!ok) break;
       tc_fence_after_sync();
       uint32_t s[2][32], dp[2][32];
@@ -491,28 +551,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       reg_fence(s[1]);
       reg_fence(dp[0]);
       reg_fence(dp[1]);
-      // allowed query columns of this group: lo .. hi (causal: query >= key; query < S)
+      // allowed query columns of this half: lo .. hi (causal: query >= key; query < S)
       const int c0 = i * kTileRows + 64 * g;
       const int hi = p.S - 1 - c0;
       int lo = CAUSAL ? gk - c0 : 0;
       if (gk >= p.S) lo = 64;  // key row past the end: nothing
       const bool edge = lo > 0 || hi < 63;
-      const uint32_t stat = sb + L::kStatOff + st * L::kStatBytes + 4 * 64 * g;
+      // (lse·log2e, delta) of this half's 64 query columns, two columns per load
+      const float4* stat = reinterpret_cast<const float4*>(
+          smem_gen + L::kStatOff + st * L::kStatBytes + 8 * 64 * g);
       uint32_t ppk[32], dpk[32];
 #pragma unroll
       for (int e2 = 0; e2 < 32; ++e2) {
         const int h = e2 >> 4;
         const int e = (2 * e2) & 31;
-        const float2 l2 = ld_shared_f32x2(stat + 8 * e2);                        // lse·log2e
-        const float2 dl = ld_shared_f32x2(stat + kTileRows * 4 + 8 * e2);        // delta
-        float p0 = ex2_approx(fmaf(__uint_as_float(s[h][e]), sl2, -l2.x));
-        float p1 = ex2_approx(fmaf(__uint_as_float(s[h][e + 1]), sl2, -l2.y));
+        const float4 sd = stat[e2];  // lse2[c], delta[c], lse2[c+1], delta[c+1]
+        float p0 = ex2_approx(fmaf(__uint_as_float(s[h][e]), sl2, -sd.x));
+        float p1 = ex2_approx(fmaf(__uint_as_float(s[h][e + 1]), sl2, -sd.z));
         if (edge) {
           if (2 * e2 < lo || 2 * e2 > hi) p0 = 0.f;
           if (2 * e2 + 1 < lo || 2 * e2 + 1 > hi) p1 = 0.f;
         }
-        const float ds0 = p0 * (__uint_as_float(dp[h][e]) - dl.x);
-        const float ds1 = p1 * (__uint_as_float(dp[h][e + 1]) - dl.y);
+        const float ds0 = p0 * (__uint_as_float(dp[h][e]) - sd.y);
+        const float ds1 = p1 * (__uint_as_float(dp[h][e + 1]) - sd.w);
         ppk[e2] = pack_bf16x2(p0, p1);
         dpk[e2] = pack_bf16x2(ds0, ds1);
       }
@@ -520,10 +581,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       tmem_st_32x32b_x32(tP, dpk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(bar(L::kPFull));
+      mbar_arrive(bar(L::kPFull + g));
     }
 
-    // ---- epilogue: group 0 stores dV (staged in V_j's buffer), group 1 dK · scale
+    // ---- epilogue: warpgroup 0 stores dV (staged in V_j's buffer), 1 stores dK · scale
     if (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kOFull), 0, ctl, kSiteKvElemO));
     }
@@ -579,8 +640,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
         const int c = lane + 32 * t;
         const int q = i * kTileRows + c;
         const bool in = q < p.S;
-        st_shared_f32(stat + 4 * c, in ? p.lse[row0 + q] * kLog2e : 0.f);
-        st_shared_f32(stat + kTileRows * 4 + 4 * c, in ? p.delta[row0 + q] : 0.f);
+        st_shared_f32x2(stat + 8 * c, in ? p.lse[row0 + q] * kLog2e : 0.f,
+                        in ? p.delta[row0 + q] : 0.f);
       }
       __syncwarp();
       if (lane == 0) {
@@ -612,9 +673,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
     const bool leader = elect_one();
-    constexpr uint32_t kIdescS = instr_desc_bf16(kTileRows, kTileRows, false, false);
+    constexpr uint32_t kIdescSP = instr_desc_bf16(kTileRows, 64, false, false);  // 64 queries
     constexpr uint32_t kIdescG = instr_desc_bf16(kTileRows, D, false, true);
     constexpr uint32_t kTileUnits = L::kTile >> 4;
+    constexpr uint32_t kHalfUnits = (64 * 128) >> 4;  // 64 rows of a 128-byte-row block
     const uint64_t dk = smem_desc_sw128(sb + L::kKOff, 16, 1024);
     const uint64_t dv = smem_desc_sw128(sb + L::kVOff, 16, 1024);
     const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
@@ -624,40 +686,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
     auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
       return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
     };
+    // SP(it, h): Sᵀ_h = K_j · Q_i[64h, 64h+64)ᵀ and dPᵀ_h = V_j · dO_i[64h, 64h+64)ᵀ
+    auto issue_sp = [&](int st, int h) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ss(tmem_base + 128 * h, dk + off, dq + st * kTileUnits + h * kHalfUnits + off,
+               kIdescSP, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ss(tmem_base + 128 * h + 64, dv + off, ddo + st * kTileUnits + h * kHalfUnits + off,
+               kIdescSP, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(L::kSFull + h));
+    };
+    // G(it, h): dV += Pᵀ_h · dO_i[64h, 64h+64), dK += dSᵀ_h · Q_i[64h, 64h+64)
+    auto issue_g = [&](int st, int h, bool first) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t a = 128 * h + kk * 8;
+        const uint32_t b = st * kTileUnits + (4 * h + kk) * (2048 >> 4);
+        const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+        mma_ts(tmem_base + 256, tmem_base + a, ddo_mn + b, kIdescG, acc);
+        mma_ts(tmem_base + 256 + D, tmem_base + a + 64, dq_mn + b, kIdescG, acc);
+      }
+    };
+
     bool ok = wait_warp(bar(L::kKVFull), 0, kSiteKvMmaKV);
-    for (int it = 0; it < nq && ok; ++it) {
-      const int st = it % L::kStages;
-      ok = wait_warp(bar(L::kFull + st), (it / L::kStages) & 1, kSiteKvMmaQ | (it & 0xff));
-      if (!ok) break;
+    if (ok) ok = wait_warp(bar(L::kFull + 0), 0, kSiteKvMmaQ);
+    if (ok) {
       tc_fence_after_sync();
       if (leader) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // Sᵀ = K_j · Q_iᵀ
-          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem_base, dk + off, dq + st * kTileUnits + off, kIdescS, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dPᵀ = V_j · dO_iᵀ
-          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem_base + 128, dv + off, ddo + st * kTileUnits + off, kIdescS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kSFull));
+        issue_sp(0, 0);
+        issue_sp(0, 1);
       }
       __syncwarp();
-      ok = wait_warp(bar(L::kPFull), it & 1, kSiteKvMmaP | (it & 0xff));
+    }
+    for (int it = 0; it < nq && ok; ++it) {
+      const int st = it % L::kStages;
+      const bool more = it + 1 < nq;
+      const int stn = (it + 1) % L::kStages;
+      ok = wait_warp(bar(L::kPFull + 0), it & 1, kSiteKvMmaP | (it & 0x7f));
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) issue_g(st, 0, it == 0);
+      __syncwarp();
+      if (more) {
+        ok = wait_warp(bar(L::kFull + stn), ((it + 1) / L::kStages) & 1, kSiteKvMmaQ | (it & 0xff));
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (leader) issue_sp(stn, 0);
+        __syncwarp();
+      }
+      ok = wait_warp(bar(L::kPFull + 1), it & 1, kSiteKvMmaP | 0x80 | (it & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
       if (leader) {
-#pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk) {  // 16 query rows per step
-          const uint32_t a = 64 * (kk >> 2) + (kk & 3) * 8;
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem_base + 256, tmem_base + a, ddo_mn + st * kTileUnits + kk * (2048 >> 4),
-                 kIdescG, acc);  // dV += Pᵀ · dO_i
-          mma_ts(tmem_base + 256 + D, tmem_base + 128 + a, dq_mn + st * kTileUnits + kk * (2048 >> 4),
-                 kIdescG, acc);  // dK += dSᵀ · Q_i
-        }
-        mma_commit(bar(L::kEmpty + st));
+        issue_g(st, 1, false);
+        mma_commit(bar(L::kEmpty + st));  // Q_i, dO_i: last read by G(it, 1)
+        if (more) issue_sp(stn, 1);
       }
       __syncwarp();
     }
