@@ -19,10 +19,13 @@ from .build import LIB_PATH
 
 __all__ = ["AttnError", "load_library", "attn_fwd", "attn_fwd_bounded", "attn_fwd_staged",
            "attn_fwd_noalloc", "attn_bwd", "attn_bwd_bounded", "device_status", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
-           "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
+           "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_F16",
+           "EXPORTED_SYMBOLS"]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
 ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 3, 4, 5
+ATTN_BF16, ATTN_F16 = 0, 1
+ATTN_DEFAULT_WAIT_TIMEOUT_NS = 2_000_000_000
 
 _i64, _p, _f, _i, _u64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int, ctypes.c_uint64
 _SIGS = {
@@ -33,6 +36,8 @@ _SIGS = {
     "attn_fwd_noalloc": (_i, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _f, _i, _i, _p]),
     "attn_bwd": (_i, [_p] * 10 + [_i64, _i64, _i64, _i64, _f, _i, _p]),
     "attn_bwd_bounded": (_i, [_p] * 10 + [_i64, _i64, _i64, _i64, _f, _i, _u64, _p]),
+    "attn_fwd_ex": (_i, [_p] * 5 + [_i64, _i64, _i64, _i64, _f, _i, _i, _u64, _p]),
+    "attn_bwd_ex": (_i, [_p] * 10 + [_i64, _i64, _i64, _i64, _f, _i, _i, _u64, _p]),
     "attn_device_status": (_i, [_p]),
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_abi_version": (_i, []),
@@ -82,16 +87,23 @@ def _stream_handle(device: torch.device, stream) -> int:
     return int(s.cuda_stream)
 
 
-def _check_qkv(q, k, v):
+_DTYPES = {torch.bfloat16: ATTN_BF16, torch.float16: ATTN_F16}
+
+
+def _check_qkv(q, k, v, allow_f16=False):
+    """Checks q, k, v; returns the library's dtype code for them."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda:
             raise TypeError(f"{name} must be a CUDA tensor")
-        if t.dtype != torch.bfloat16:
-            raise TypeError(f"{name} must be bfloat16")
+        if t.dtype != torch.bfloat16 and not (allow_f16 and t.dtype == torch.float16):
+            raise TypeError(f"{name} must be bfloat16" + (" or float16" if allow_f16 else ""))
         if t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous [B, H, S, D] tensor")
     if not (q.shape == k.shape == v.shape) or not (q.device == k.device == v.device):
         raise ValueError("q, k, v must share shape and device")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    return _DTYPES[q.dtype]
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
@@ -103,8 +115,9 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | N
 
 def attn_fwd_bounded(q, k, v, scale=None, causal=True, out=None, lse=None, stream=None,
                      wait_timeout_ns: int | None = None):
-    """attn_fwd with an explicit bound on every in-kernel wait (None = library default)."""
-    _check_qkv(q, k, v)
+    """attn_fwd with an explicit bound on every in-kernel wait (None = library default).
+    q, k, v may be bfloat16 or float16; out has their dtype."""
+    dt = _check_qkv(q, k, v, allow_f16=True)
     B, H, S, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
@@ -112,8 +125,8 @@ def attn_fwd_bounded(q, k, v, scale=None, causal=True, out=None, lse=None, strea
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    if out.dtype != torch.bfloat16 or out.shape != q.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if out.dtype != q.dtype or out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q, of its dtype")
     if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor")
     lib = load_library()
@@ -121,7 +134,10 @@ def attn_fwd_bounded(q, k, v, scale=None, causal=True, out=None, lse=None, strea
             B, H, S, D, float(scale), 1 if causal else 0)
     with torch.cuda.device(q.device):
         st = _stream_handle(q.device, stream)
-        if wait_timeout_ns is None:
+        if dt == ATTN_F16:
+            tmo = ATTN_DEFAULT_WAIT_TIMEOUT_NS if wait_timeout_ns is None else int(wait_timeout_ns)
+            rc = lib.attn_fwd_ex(*args, dt, tmo, st)
+        elif wait_timeout_ns is None:
             rc = lib.attn_fwd(*args, st)
         else:
             rc = lib.attn_fwd_bounded(*args, int(wait_timeout_ns), st)
@@ -184,13 +200,14 @@ def attn_bwd(q, k, v, out, lse, dout, scale=None, causal=True, dq=None, dk=None,
 
 def attn_bwd_bounded(q, k, v, out, lse, dout, scale=None, causal=True, dq=None, dk=None, dv=None,
                      delta=None, stream=None, wait_timeout_ns: int | None = None):
-    """attn_bwd with an explicit bound on every in-kernel wait (None = library default)."""
-    _check_qkv(q, k, v)
+    """attn_bwd with an explicit bound on every in-kernel wait (None = library default).
+    The 16-bit tensors may be bfloat16 or float16 (all the same)."""
+    dt = _check_qkv(q, k, v, allow_f16=True)
     B, H, S, D = q.shape
     for name, t in (("out", out), ("dout", dout)):
-        if (not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.shape != q.shape
+        if (not isinstance(t, torch.Tensor) or t.dtype != q.dtype or t.shape != q.shape
                 or not t.is_contiguous() or t.device != q.device):
-            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q on its device")
+            raise ValueError(f"{name} must be a contiguous tensor shaped like q, of its dtype and device")
     if (not isinstance(lse, torch.Tensor) or lse.dtype != torch.float32 or lse.shape != (B, H, S)
             or not lse.is_contiguous() or lse.device != q.device):
         raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor on q's device")
@@ -201,8 +218,8 @@ def attn_bwd_bounded(q, k, v, out, lse, dout, scale=None, causal=True, dq=None, 
     dv = torch.empty_like(q) if dv is None else dv
     delta = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if delta is None else delta
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        if t.dtype != torch.bfloat16 or t.shape != q.shape or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+        if t.dtype != q.dtype or t.shape != q.shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor shaped like q, of its dtype")
     if delta.dtype != torch.float32 or delta.shape != (B, H, S) or not delta.is_contiguous():
         raise ValueError("delta must be a contiguous fp32 [B, H, S] tensor")
     lib = load_library()
@@ -211,7 +228,10 @@ def attn_bwd_bounded(q, k, v, out, lse, dout, scale=None, causal=True, dq=None, 
             B, H, S, D, float(scale), 1 if causal else 0)
     with torch.cuda.device(q.device):
         st = _stream_handle(q.device, stream)
-        if wait_timeout_ns is None:
+        if dt == ATTN_F16:
+            tmo = ATTN_DEFAULT_WAIT_TIMEOUT_NS if wait_timeout_ns is None else int(wait_timeout_ns)
+            rc = lib.attn_bwd_ex(*args, dt, tmo, st)
+        elif wait_timeout_ns is None:
             rc = lib.attn_bwd(*args, st)
         else:
             rc = lib.attn_bwd_bounded(*args, int(wait_timeout_ns), st)

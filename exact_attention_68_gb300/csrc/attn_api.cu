@@ -96,13 +96,13 @@ attn_status_t device_state(int* dev_out, DeviceState** st_out) {
 }
 
 attn_status_t launch(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B,
-                     int64_t H, int64_t S, int64_t D, float scale, int causal,
+                     int64_t H, int64_t S, int64_t D, float scale, int causal, bool f16,
                      uint64_t timeout_ns, cudaStream_t stream) {
   int dev = -1;
   DeviceState* st = nullptr;
   attn_status_t s = device_state(&dev, &st);
   if (s != ATTN_OK) return s;
-  return ea::launch_with_status(q, k, v, out, lse, B, H, S, D, scale, causal, timeout_ns,
+  return ea::launch_with_status(q, k, v, out, lse, B, H, S, D, scale, causal, f16, timeout_ns,
                                 st->status, stream);
 }
 
@@ -127,15 +127,15 @@ attn_status_t current_status_words(int** status) {
 
 attn_status_t launch_with_status(const void* q, const void* k, const void* v, void* out,
                                  float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
-                                 float scale, int causal, uint64_t timeout_ns, int* status,
-                                 cudaStream_t stream) {
+                                 float scale, int causal, bool f16, uint64_t timeout_ns,
+                                 int* status, cudaStream_t stream) {
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   const int64_t BH = B * H;
-  if (!encode_bhsd_bf16(&p.tm_q, q, BH, S, D, kBlockM) ||
-      !encode_bhsd_bf16(&p.tm_k, k, BH, S, D, kBlockN) ||
-      !encode_bhsd_bf16(&p.tm_v, v, BH, S, D, kBlockN) ||
-      !encode_bhsd_bf16(&p.tm_o, out, BH, S, D, 32))
+  if (!encode_bhsd_16bit(&p.tm_q, q, BH, S, D, kBlockM, f16) ||
+      !encode_bhsd_16bit(&p.tm_k, k, BH, S, D, kBlockN, f16) ||
+      !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, kBlockN, f16) ||
+      !encode_bhsd_16bit(&p.tm_o, out, BH, S, D, 32, f16))
     return ATTN_ERR_CUDA;
   p.lse = lse;
   p.status = status;
@@ -151,7 +151,7 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
   p.sched = plan_schedule(BH, p.n_units, S, D, causal != 0, kL2GroupBytes, sms);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout_ns;
-  if (fwd_launch(p, static_cast<int>(D), causal != 0, stream) != cudaSuccess) {
+  if (fwd_launch(p, static_cast<int>(D), causal != 0, f16, stream) != cudaSuccess) {
     (void)cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
@@ -167,7 +167,17 @@ attn_status_t attn_fwd_bounded(const void* q, const void* k, const void* v, void
                                uint64_t wait_timeout_ns, cudaStream_t stream) {
   attn_status_t s = validate(q, k, v, out, lse, B, H, S, D, scale, causal);
   if (s != ATTN_OK) return s;
-  return launch(q, k, v, out, lse, B, H, S, D, scale, causal, wait_timeout_ns, stream);
+  return launch(q, k, v, out, lse, B, H, S, D, scale, causal, false, wait_timeout_ns, stream);
+}
+
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                          int64_t B, int64_t H, int64_t S, int64_t D, float scale, int causal,
+                          attn_dtype_t dtype, uint64_t wait_timeout_ns, cudaStream_t stream) {
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_INVALID_ARG;
+  attn_status_t s = validate(q, k, v, out, lse, B, H, S, D, scale, causal);
+  if (s != ATTN_OK) return s;
+  return launch(q, k, v, out, lse, B, H, S, D, scale, causal, dtype == ATTN_F16, wait_timeout_ns,
+                stream);
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -191,7 +201,8 @@ attn_status_t attn_fwd_staged(const void* q_h, const void* k_h, const void* v_h,
       cudaMemcpyAsync(k_d, k_h, nt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaMemcpyAsync(v_d, v_h, nt, cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  s = launch(q_d, k_d, v_d, out_d, lse_d, B, H, S, D, scale, causal, kDefaultWaitTimeoutNs, stream);
+  s = launch(q_d, k_d, v_d, out_d, lse_d, B, H, S, D, scale, causal, false, kDefaultWaitTimeoutNs,
+             stream);
   if (s != ATTN_OK) return s;
   if (cudaMemcpyAsync(out_h, out_d, nt, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
       cudaMemcpyAsync(lse_h, lse_d, nl, cudaMemcpyDeviceToHost, stream) != cudaSuccess)

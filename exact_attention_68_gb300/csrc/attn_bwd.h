@@ -21,8 +21,8 @@ struct BwdParams {
   CUtensorMap tm_dq;  // dq, box 64 x 32 rows (one warp's rows)
   CUtensorMap tm_dk;  // dk, same
   CUtensorMap tm_dv;  // dv, same
-  const uint16_t* out;   // bf16 [B·H, S, D]: forward output (rows read for delta)
-  const uint16_t* dout;  // bf16 [B·H, S, D]
+  const uint16_t* out;   // 16-bit [B·H, S, D]: forward output (rows read for delta)
+  const uint16_t* dout;  // 16-bit [B·H, S, D]
   const float* lse;      // [B·H, S]: natural-log logsumexp saved by the forward
   float* delta;          // [B·H, S]: rowsum(dout ⊙ out), written by the dq kernel
   int* status;           // device status word pair (error bits, first wait site)
@@ -34,7 +34,7 @@ struct BwdParams {
 };
 
 // Launches the dq kernel (which also writes delta) and then the dk/dv kernel
-// on `stream`.
-cudaError_t bwd_launch(const BwdParams& p, int D, bool causal, cudaStream_t stream);
+// on `stream`.  f16: the 16-bit tensors are fp16 (else bf16).
+cudaError_t bwd_launch(const BwdParams& p, int D, bool causal, bool f16, cudaStream_t stream);
 
 }  // namespace ea

@@ -52,11 +52,13 @@ attn_status_t validate_bwd(const void* q, const void* k, const void* v, const vo
 
 extern "C" {
 
-attn_status_t attn_bwd_bounded(const void* q, const void* k, const void* v, const void* out,
-                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                               float* delta, int64_t B, int64_t H, int64_t S, int64_t D,
-                               float scale, int causal, uint64_t wait_timeout_ns,
-                               cudaStream_t stream) {
+attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          float* delta, int64_t B, int64_t H, int64_t S, int64_t D, float scale,
+                          int causal, attn_dtype_t dtype, uint64_t wait_timeout_ns,
+                          cudaStream_t stream) {
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_INVALID_ARG;
+  const bool f16 = dtype == ATTN_F16;
   attn_status_t s = validate_bwd(q, k, v, out, lse, dout, dq, dk, dv, delta, B, H, S, D, scale,
                                  causal);
   if (s != ATTN_OK) return s;
@@ -66,13 +68,13 @@ attn_status_t attn_bwd_bounded(const void* q, const void* k, const void* v, cons
   ea::BwdParams p;
   std::memset(&p, 0, sizeof(p));
   const int64_t BH = B * H;
-  if (!ea::encode_bhsd_bf16(&p.tm_q, q, BH, S, D, 128) ||
-      !ea::encode_bhsd_bf16(&p.tm_k, k, BH, S, D, 128) ||
-      !ea::encode_bhsd_bf16(&p.tm_v, v, BH, S, D, 128) ||
-      !ea::encode_bhsd_bf16(&p.tm_do, dout, BH, S, D, 128) ||
-      !ea::encode_bhsd_bf16(&p.tm_dq, dq, BH, S, D, 32) ||
-      !ea::encode_bhsd_bf16(&p.tm_dk, dk, BH, S, D, 32) ||
-      !ea::encode_bhsd_bf16(&p.tm_dv, dv, BH, S, D, 32))
+  if (!ea::encode_bhsd_16bit(&p.tm_q, q, BH, S, D, 128, f16) ||
+      !ea::encode_bhsd_16bit(&p.tm_k, k, BH, S, D, 128, f16) ||
+      !ea::encode_bhsd_16bit(&p.tm_v, v, BH, S, D, 128, f16) ||
+      !ea::encode_bhsd_16bit(&p.tm_do, dout, BH, S, D, 128, f16) ||
+      !ea::encode_bhsd_16bit(&p.tm_dq, dq, BH, S, D, 32, f16) ||
+      !ea::encode_bhsd_16bit(&p.tm_dk, dk, BH, S, D, 32, f16) ||
+      !ea::encode_bhsd_16bit(&p.tm_dv, dv, BH, S, D, 32, f16))
     return ATTN_ERR_CUDA;
   p.out = static_cast<const uint16_t*>(out);
   p.dout = static_cast<const uint16_t*>(dout);
@@ -86,11 +88,20 @@ attn_status_t attn_bwd_bounded(const void* q, const void* k, const void* v, cons
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = wait_timeout_ns;
-  if (ea::bwd_launch(p, static_cast<int>(D), causal != 0, stream) != cudaSuccess) {
+  if (ea::bwd_launch(p, static_cast<int>(D), causal != 0, f16, stream) != cudaSuccess) {
     (void)cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
   return ATTN_OK;
+}
+
+attn_status_t attn_bwd_bounded(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               float* delta, int64_t B, int64_t H, int64_t S, int64_t D,
+                               float scale, int causal, uint64_t wait_timeout_ns,
+                               cudaStream_t stream) {
+  return attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, delta, B, H, S, D, scale, causal,
+                     ATTN_BF16, wait_timeout_ns, stream);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* out,

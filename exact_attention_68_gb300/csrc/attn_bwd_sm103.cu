@@ -42,6 +42,7 @@
 // of the half's gradient MMAs.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "attn_bwd.h"
@@ -67,15 +68,27 @@ enum : int {
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
-__device__ __forceinline__ float dot_bf16x8(uint4 a, uint4 b) {
-  float s = bf16_lo(a.x) * bf16_lo(b.x);
-  s = fmaf(bf16_hi(a.x), bf16_hi(b.x), s);
-  s = fmaf(bf16_lo(a.y), bf16_lo(b.y), s);
-  s = fmaf(bf16_hi(a.y), bf16_hi(b.y), s);
-  s = fmaf(bf16_lo(a.z), bf16_lo(b.z), s);
-  s = fmaf(bf16_hi(a.z), bf16_hi(b.z), s);
-  s = fmaf(bf16_lo(a.w), bf16_lo(b.w), s);
-  s = fmaf(bf16_hi(a.w), bf16_hi(b.w), s);
+__device__ __forceinline__ float2 f16x2_to_f32(uint32_t x) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&x));
+}
+
+// Σ a_e·b_e over 8 packed 16-bit values (fp16 if F16, else bf16), in fp32.
+template <bool F16>
+__device__ __forceinline__ float dot8(uint4 a, uint4 b) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+  float s = 0.f;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    if constexpr (F16) {
+      const float2 x = f16x2_to_f32(av[t]), y = f16x2_to_f32(bv[t]);
+      s = fmaf(x.x, y.x, s);
+      s = fmaf(x.y, y.y, s);
+    } else {
+      s = fmaf(bf16_lo(av[t]), bf16_lo(bv[t]), s);
+      s = fmaf(bf16_hi(av[t]), bf16_hi(bv[t]), s);
+    }
+  }
   return s;
 }
 
@@ -94,6 +107,7 @@ __device__ __forceinline__ void st_shared_f32x2(uint32_t addr, float a, float b)
 // One warp's 32 rows × 64 columns of an fp32 TMEM accumulator, times `mul`,
 // to bf16 in the 128-byte-swizzled staging block `chunk_base` (row = TMEM
 // lane), then one TMA store of the warp's rows.  Only lane 0 issues the store.
+template <bool F16>
 __device__ __forceinline__ void store_chunk(uint32_t tmem_col, uint32_t chunk_base, int row,
                                             float mul, const CUtensorMap* map, int x, int y0,
                                             int z, int wq, int lane) {
@@ -110,7 +124,7 @@ __device__ __forceinline__ void store_chunk(uint32_t tmem_col, uint32_t chunk_ba
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        w[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * mul,
+        w[e] = pack_x2<F16>(__uint_as_float(o[q4 * 8 + 2 * e]) * mul,
                            __uint_as_float(o[q4 * 8 + 2 * e + 1]) * mul);
       st_shared_v4(addr, w[0], w[1], w[2], w[3]);
     }
@@ -150,7 +164,7 @@ struct DqLayout {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = DqLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -218,7 +232,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       const uint4* o4 = reinterpret_cast<const uint4*>(p.out + base) + g * (D / 16);
       const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + base) + g * (D / 16);
 #pragma unroll
-      for (int u = 0; u < D / 16; ++u) part += dot_bf16x8(__ldg(o4 + u), __ldg(d4 + u));
+      for (int u = 0; u < D / 16; ++u) part += dot8<F16>(__ldg(o4 + u), __ldg(d4 + u));
     }
     st_shared_f32(sb + L::kPartOff + 4 * (g * kTileRows + row), part);
     named_bar_sync(1, 256);
@@ -263,7 +277,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
         }
         const float ds0 = p0 * (__uint_as_float(dp[h][e]) - delta);
         const float ds1 = p1 * (__uint_as_float(dp[h][e + 1]) - delta);
-        pk[e2] = pack_bf16x2(ds0, ds1);
+        pk[e2] = pack_x2<F16>(ds0, ds1);
       }
       tmem_st_32x32b_x32(tS, pk);
       tmem_st_wait();
@@ -278,7 +292,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     if (ok) {
       tc_fence_after_sync();
       for (int c = g; c < L::kChunks; c += 2)
-        store_chunk(tQ + c * 64, sb + L::kQOff + c * kChunkBytes, row, p.scale, &p.tm_dq, c * 64,
+        store_chunk<F16>(tQ + c * 64, sb + L::kQOff + c * kChunkBytes, row, p.scale, &p.tm_dq, c * 64,
                     i * kTileRows, bh, wq, lane);
       if (lane == 0) {
         tma_store_commit();
@@ -348,8 +362,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
     const bool leader = elect_one();
-    constexpr uint32_t kIdescSP = instr_desc_bf16(kTileRows, 64, false, false);  // 64 keys
-    constexpr uint32_t kIdescQ = instr_desc_bf16(kTileRows, D, false, true);
+    constexpr uint32_t kIdescSP = instr_desc_16bit(kTileRows, 64, false, false, F16);  // 64 keys
+    constexpr uint32_t kIdescQ = instr_desc_16bit(kTileRows, D, false, true, F16);
     constexpr uint32_t kTileUnits = L::kTile >> 4;
     constexpr uint32_t kHalfUnits = (64 * 128) >> 4;  // 64 rows of a 128-byte-row block
     const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
@@ -477,7 +491,7 @@ struct KvLayout {
   static_assert(256 + 2 * D <= 512, "TMEM budget exceeded");
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using L = KvLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -574,8 +588,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
         }
         const float ds0 = p0 * (__uint_as_float(dp[h][e]) - sd.y);
         const float ds1 = p1 * (__uint_as_float(dp[h][e + 1]) - sd.w);
-        ppk[e2] = pack_bf16x2(p0, p1);
-        dpk[e2] = pack_bf16x2(ds0, ds1);
+        ppk[e2] = pack_x2<F16>(p0, p1);
+        dpk[e2] = pack_x2<F16>(ds0, ds1);
       }
       tmem_st_32x32b_x32(tS, ppk);
       tmem_st_32x32b_x32(tP, dpk);
@@ -596,7 +610,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       const float mul = g == 0 ? 1.f : p.scale;
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
-        store_chunk(tAcc + c * 64, stage + c * kChunkBytes, r, mul, map, c * 64, j * kTileRows, bh,
+        store_chunk<F16>(tAcc + c * 64, stage + c * kChunkBytes, r, mul, map, c * 64, j * kTileRows, bh,
                     wq, lane);
       if (lane == 0) {
         tma_store_commit();
@@ -673,8 +687,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
     const bool leader = elect_one();
-    constexpr uint32_t kIdescSP = instr_desc_bf16(kTileRows, 64, false, false);  // 64 queries
-    constexpr uint32_t kIdescG = instr_desc_bf16(kTileRows, D, false, true);
+    constexpr uint32_t kIdescSP = instr_desc_16bit(kTileRows, 64, false, false, F16);  // 64 queries
+    constexpr uint32_t kIdescG = instr_desc_16bit(kTileRows, D, false, true, F16);
     constexpr uint32_t kTileUnits = L::kTile >> 4;
     constexpr uint32_t kHalfUnits = (64 * 128) >> 4;  // 64 rows of a 128-byte-row block
     const uint64_t dk = smem_desc_sw128(sb + L::kKOff, 16, 1024);
@@ -765,10 +779,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream) {
-  auto kdq = attn_bwd_dq_kernel<D, CAUSAL>;
-  auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL>;
+  auto kdq = attn_bwd_dq_kernel<D, CAUSAL, F16>;
+  auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL, F16>;
   cudaError_t e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DqLayout<D>::kAlloc);
   if (e != cudaSuccess) return e;
@@ -782,11 +796,17 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <bool F16>
+cudaError_t launch_typed(const BwdParams& p, int D, bool causal, cudaStream_t stream) {
+  if (D == 64)
+    return causal ? launch_impl<64, true, F16>(p, stream) : launch_impl<64, false, F16>(p, stream);
+  return causal ? launch_impl<128, true, F16>(p, stream) : launch_impl<128, false, F16>(p, stream);
+}
+
 }  // namespace
 
-cudaError_t bwd_launch(const BwdParams& p, int D, bool causal, cudaStream_t stream) {
-  if (D == 64) return causal ? launch_impl<64, true>(p, stream) : launch_impl<64, false>(p, stream);
-  return causal ? launch_impl<128, true>(p, stream) : launch_impl<128, false>(p, stream);
+cudaError_t bwd_launch(const BwdParams& p, int D, bool causal, bool f16, cudaStream_t stream) {
+  return f16 ? launch_typed<true>(p, D, causal, stream) : launch_typed<false>(p, D, causal, stream);
 }
 
 }  // namespace ea

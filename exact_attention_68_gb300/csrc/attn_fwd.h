@@ -43,6 +43,7 @@ struct FwdParams {
 size_t fwd_smem_bytes(int D);
 
 // Sets per-kernel attributes (once per device) and launches one forward.
-cudaError_t fwd_launch(const FwdParams& p, int D, bool causal, cudaStream_t stream);
+// f16: q, k, v, out are fp16 (else bf16).
+cudaError_t fwd_launch(const FwdParams& p, int D, bool causal, bool f16, cudaStream_t stream);
 
 }  // namespace ea

@@ -87,7 +87,7 @@ enum : int {
   kSiteMmaV = 0x500, kSiteMmaP = 0x600, kSiteSoftS = 0x700, kSiteSoftO = 0x800
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const float p0 = ex2_approx(x.x);
           const float p1 = ex2_approx(x.y);
           rs2[i & 3] = __fadd2_rn(rs2[i & 3], make_float2(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+          pk[i] = pack_x2<F16>(p0, p1);
         }
         tmem_st_32x32b_x32(tS + h * 32, pk);
       };
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const float rs = rs_a.x + rs_a.y;
       // the tile's largest p, computed exactly as in P, and its bf16 value
       const float pmax = ex2_approx(fmaf(mx, sl2, (m == -INFINITY) ? 0.f : -m));
-      const float pmax_q = __uint_as_float(pack_bf16x2(pmax, 0.f) << 16);
+      const float pmax_q = round_to_x<F16>(pmax);
       l = l * alpha + rs;
       lq = lq * alpha + (rs + (pmax_q - pmax));
       // correction: rescale this row of O when its reference max moved.  PV_{j-1}
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
+              w[e] = pack_x2<F16>(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
                                  __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
             st_shared_v4(addr, w[0], w[1], w[2], w[3]);
           }
@@ -402,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // warp-uniform); one elected lane issues every tcgen05.mma and commit.
       const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
       const bool leader = elect_one();
-      constexpr uint32_t kIdescS = instr_desc_bf16(kBlockM, kBlockN, false, false);
-      constexpr uint32_t kIdescO = instr_desc_bf16(kBlockM, D, false, true);
+      constexpr uint32_t kIdescS = instr_desc_16bit(kBlockM, kBlockN, false, false, F16);
+      constexpr uint32_t kIdescO = instr_desc_16bit(kBlockM, D, false, true, F16);
       // Descriptor bases; a K step or a stage only moves the start-address
       // field (16-byte units; no carry out of it: smem < 256 KB).
       const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
@@ -505,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
   using L = Layout<D>;
-  auto kern = attn_fwd_kernel<D, CAUSAL>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, F16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.B * p.H * p.n_units;
@@ -526,9 +526,15 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
 
 size_t fwd_smem_bytes(int D) { return D == 64 ? Layout<64>::kAlloc : Layout<128>::kAlloc; }
 
-cudaError_t fwd_launch(const FwdParams& p, int D, bool causal, cudaStream_t stream) {
-  if (D == 64) return causal ? launch_impl<64, true>(p, stream) : launch_impl<64, false>(p, stream);
-  return causal ? launch_impl<128, true>(p, stream) : launch_impl<128, false>(p, stream);
+template <bool F16>
+static cudaError_t launch_typed(const FwdParams& p, int D, bool causal, cudaStream_t stream) {
+  if (D == 64)
+    return causal ? launch_impl<64, true, F16>(p, stream) : launch_impl<64, false, F16>(p, stream);
+  return causal ? launch_impl<128, true, F16>(p, stream) : launch_impl<128, false, F16>(p, stream);
+}
+
+cudaError_t fwd_launch(const FwdParams& p, int D, bool causal, bool f16, cudaStream_t stream) {
+  return f16 ? launch_typed<true>(p, D, causal, stream) : launch_typed<false>(p, D, causal, stream);
 }
 
 }  // namespace ea

@@ -17,10 +17,11 @@ attn_status_t validate_args(const void* q, const void* k, const void* v, const v
 
 // Encodes the tensor maps and launches the forward with `status` (device
 // int[2]: error bits, first wait site that ran out) as its status words.
+// f16: the 16-bit tensors are fp16 (else bf16).
 attn_status_t launch_with_status(const void* q, const void* k, const void* v, void* out,
                                  float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
-                                 float scale, int causal, uint64_t timeout_ns, int* status,
-                                 cudaStream_t stream);
+                                 float scale, int causal, bool f16, uint64_t timeout_ns,
+                                 int* status, cudaStream_t stream);
 
 // The current device's status word pair (allocated on first use), after the
 // architecture check.

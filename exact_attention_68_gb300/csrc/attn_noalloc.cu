@@ -85,8 +85,8 @@ extern "C" attn_status_t attn_fwd_noalloc(const void* q, const void* k, const vo
   if (s != ATTN_OK) return s;
   // The array keeps the previous call's words: clear them for this call.
   if (cudaMemsetAsync(scratch, 0, kScratchNeedBytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-  s = ea::launch_with_status(q, k, v, out, lse, B, H, S, D, scale, causal, kWaitTimeoutNs, scratch,
-                             stream);
+  s = ea::launch_with_status(q, k, v, out, lse, B, H, S, D, scale, causal, /*f16=*/false,
+                             kWaitTimeoutNs, scratch, stream);
   if (s != ATTN_OK || !check_status) return s;
   int words[2] = {0, 0};
   if (cudaMemcpyAsync(words, scratch, sizeof(words), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||

@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda.h>  // CUtensorMap
 
 namespace ea {
@@ -345,6 +346,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Pack two fp32 into f16x2 (round to nearest even): lo → bits 0-15, hi → 16-31.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The 16-bit input type of the tensor-core operands: fp16 (F16) or bf16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_x2(float lo, float hi) {
+  if constexpr (F16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
+// x rounded to the 16-bit type (nearest even) and back to fp32.
+template <bool F16>
+__device__ __forceinline__ float round_to_x(float x) {
+  const uint32_t v = pack_x2<F16>(x, 0.f) & 0xffffu;
+  if constexpr (F16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v)));
+  } else {
+    return __uint_as_float(v << 16);
+  }
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

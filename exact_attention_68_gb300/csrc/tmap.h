@@ -27,21 +27,28 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 3-D map (D, S, BH) of a contiguous bf16 [BH, S, D] tensor with a box of
+// 3-D map (D, S, BH) of a contiguous 16-bit (fp16 if f16, else bf16)
+// [BH, S, D] tensor with a box of
 // 64 columns x box_rows rows x 1, 128-byte swizzle.  Rows past S read as zero
 // and are not written by stores, so tiles never cross into the next head.
-inline bool encode_bhsd_bf16(CUtensorMap* map, const void* base, int64_t BH, int64_t S, int64_t D,
-                             uint32_t box_rows) {
+inline bool encode_bhsd_16bit(CUtensorMap* map, const void* base, int64_t BH, int64_t S, int64_t D,
+                              uint32_t box_rows, bool f16) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)(D * 2), (cuuint64_t)(S * D * 2)};
   cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+inline bool encode_bhsd_bf16(CUtensorMap* map, const void* base, int64_t BH, int64_t S, int64_t D,
+                             uint32_t box_rows) {
+  return encode_bhsd_16bit(map, base, BH, S, D, box_rows, false);
 }
 
 }  // namespace ea

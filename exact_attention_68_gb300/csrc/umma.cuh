@@ -31,11 +31,18 @@ __host__ __device__ constexpr uint64_t smem_desc_sw128(uint32_t saddr, uint32_t 
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// A, B both fp16 (f16 = true, format 0) or both bf16 (format 1) -> f32, dense.
+__host__ __device__ constexpr uint32_t instr_desc_16bit(int M, int N, bool a_mn_major,
+                                                        bool b_mn_major, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // bf16 x bf16 -> f32, dense.
 __host__ __device__ constexpr uint32_t instr_desc_bf16(int M, int N, bool a_mn_major,
                                                        bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+  return instr_desc_16bit(M, N, a_mn_major, b_mn_major, false);
 }
 
 }  // namespace ea

@@ -62,8 +62,9 @@ def default_scale(D: int) -> float:
 
 
 def make_qkv(w: Workload | tuple, seed: int = 0, qk_std: float | None = None,
-             v_std: float | None = None):
-    """Draw (q, k, v) as contiguous CPU bf16 tensors of shape [B, H, S, D].
+             v_std: float | None = None, dtype: torch.dtype = torch.bfloat16):
+    """Draw (q, k, v) as contiguous CPU tensors of shape [B, H, S, D], rounded
+    to ``dtype`` (bf16 by default, or fp16).
 
     ``w`` is a Workload or a (B, H, S, D) tuple (then N(0,1) unless stds given).
     """
@@ -81,7 +82,7 @@ def make_qkv(w: Workload | tuple, seed: int = 0, qk_std: float | None = None,
         x = torch.randn(shape, generator=g, dtype=torch.float32)
         if std != 1.0:
             x.mul_(std)
-        out.append(x.to(torch.bfloat16).contiguous())
+        out.append(x.to(dtype).contiguous())
     return tuple(out)
 
 

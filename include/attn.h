@@ -63,6 +63,15 @@ typedef enum {
   ATTN_ERR_TIMEOUT = 5       /* a bounded in-kernel wait ran out (reported by attn_device_status) */
 } attn_status_t;
 
+/* The 16-bit type of q, k, v, out (and dout, dq, dk, dv) for the _ex entry points. */
+typedef enum {
+  ATTN_BF16 = 0,  /* bfloat16: what every other entry point uses */
+  ATTN_F16 = 1    /* IEEE half */
+} attn_dtype_t;
+
+/* The wait bound attn_fwd and attn_bwd use (nanoseconds per in-kernel wait). */
+#define ATTN_DEFAULT_WAIT_TIMEOUT_NS 2000000000ull
+
 /*
  * attn_fwd — fused attention forward on device buffers.
  *
@@ -194,6 +203,25 @@ ATTN_API attn_status_t attn_bwd_bounded(const void* q, const void* k, const void
                                         void* dq, void* dk, void* dv, float* delta, int64_t B,
                                         int64_t H, int64_t S, int64_t D, float scale, int causal,
                                         uint64_t wait_timeout_ns, cudaStream_t stream);
+
+/*
+ * attn_fwd_ex / attn_bwd_ex — attn_fwd_bounded / attn_bwd_bounded for a chosen
+ * 16-bit type.  With dtype = ATTN_F16 every 16-bit tensor (q, k, v, out; for
+ * the backward also dout, dq, dk, dv) holds IEEE half values, and the
+ * tensor-core operands the kernels form from P and dS are rounded to half as
+ * well; lse and delta stay fp32.  Layouts, ownership and errors as for the
+ * bf16 entry points; a dtype other than ATTN_BF16 or ATTN_F16 is
+ * ATTN_ERR_INVALID_ARG.  Pass ATTN_DEFAULT_WAIT_TIMEOUT_NS for the usual bound.
+ */
+ATTN_API attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* out,
+                                   float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                                   float scale, int causal, attn_dtype_t dtype,
+                                   uint64_t wait_timeout_ns, cudaStream_t stream);
+ATTN_API attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* out,
+                                   const float* lse, const void* dout, void* dq, void* dk,
+                                   void* dv, float* delta, int64_t B, int64_t H, int64_t S,
+                                   int64_t D, float scale, int causal, attn_dtype_t dtype,
+                                   uint64_t wait_timeout_ns, cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status_t status);

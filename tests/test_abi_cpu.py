@@ -145,3 +145,28 @@ def test_bwd_bounded_validates_too(lib):
     args = [A, A + T, A + 2 * T, A + 3 * T, A + 4 * T, 0, A + 6 * T, A + 7 * T, A + 8 * T,
             A + 9 * T, 1, 2, 128, 64, 0.125, 1]
     assert lib.attn_bwd_bounded(*args, 0, None) == binding.ATTN_ERR_INVALID_ARG
+
+
+def test_ex_entry_points_validate_dtype_first(lib):
+    fwd = [A, A + T, A + 2 * T, A + 3 * T, A + 4 * T, 1, 2, 128, 64, 0.125, 1]
+    assert lib.attn_fwd_ex(*fwd, 2, binding.ATTN_DEFAULT_WAIT_TIMEOUT_NS, None) == binding.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_ex(*fwd, -1, binding.ATTN_DEFAULT_WAIT_TIMEOUT_NS, None) == binding.ATTN_ERR_INVALID_ARG
+    bad = list(fwd)
+    bad[8] = 96
+    assert lib.attn_fwd_ex(*bad, binding.ATTN_F16, 0, None) == binding.ATTN_ERR_UNSUPPORTED
+    bwd = [A, A + T, A + 2 * T, A + 3 * T, A + 4 * T, A + 5 * T, A + 6 * T, A + 7 * T, A + 8 * T,
+           A + 9 * T, 1, 2, 128, 64, 0.125, 1]
+    assert lib.attn_bwd_ex(*bwd, 7, 0, None) == binding.ATTN_ERR_INVALID_ARG
+    bad = list(bwd)
+    bad[6] = A  # dq aliases q
+    assert lib.attn_bwd_ex(*bad, binding.ATTN_F16, 0, None) == binding.ATTN_ERR_INVALID_ARG
+
+
+def test_make_qkv_dtype():
+    from exact_attention_68_gb300.workloads import make_qkv
+    import torch
+    qb = make_qkv((1, 1, 8, 64), seed=3)
+    qh = make_qkv((1, 1, 8, 64), seed=3, dtype=torch.float16)
+    assert all(t.dtype == torch.bfloat16 for t in qb) and all(t.dtype == torch.float16 for t in qh)
+    # the same draws, rounded to the two types
+    assert torch.allclose(qb[0].float(), qh[0].float(), atol=2e-2 * qh[0].abs().max().item())
