@@ -272,6 +272,16 @@ def side_workloads(device, stream):
         ms = statistics.median(times)
         res[name] = {"about": w.about, "ms": ms,
                      "tflops": counted_flops(w.B, w.H, w.S, w.D, w.causal) / (ms * 1e-3) / 1e12}
+    # the default workload with fp16 inputs (attn_fwd_ex), 20 back-to-back launches
+    w = WORKLOADS[WORKLOAD]
+    q, k, v = (x.to(device) for x in make_qkv(w, seed=0, dtype=torch.float16))
+    out, lse = torch.empty_like(q), torch.empty(w.B, w.H, w.S, device=device)
+    scale = default_scale(w.D)
+    for _ in range(3):
+        binding.attn_fwd(q, k, v, scale, w.causal, out, lse)
+    ms = time_steps(lambda: binding.attn_fwd(q, k, v, scale, w.causal, out, lse), 20, stream) / 20
+    res[WORKLOAD + "_fp16"] = {"about": w.about + ", fp16 inputs", "ms": ms,
+                               "tflops": counted_flops(w.B, w.H, w.S, w.D, w.causal) / (ms * 1e-3) / 1e12}
     return res
 
 
