@@ -21,6 +21,9 @@ constexpr uint64_t kDefaultWaitTimeoutNs = 2000000000ull;  // 2 s per in-kernel 
 // 129 MB L2, so that the CTAs running at one time re-read K/V tiles from L2.
 constexpr int64_t kL2GroupBytes = 48ll << 20;
 constexpr int kMaxDevices = 64;
+// attn_fwd_staged: inputs per chunk, and the most chunks one call uses.
+constexpr int64_t kStagedChunkBytes = 48ll << 20;
+constexpr int kMaxStagedChunks = 8;
 
 struct DeviceState {
   bool ready = false;
@@ -30,6 +33,38 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// Streams and events of attn_fwd_staged on one device: uploads, kernels and
+// downloads of consecutive chunks run on three streams and overlap.  Created
+// on the first staged call on the device, kept until process exit; `mu`
+// serialises the enqueueing of staged calls, which share the events.
+struct StagedState {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t up = nullptr, run = nullptr, down = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t uploaded[kMaxStagedChunks] = {};
+  cudaEvent_t computed[kMaxStagedChunks] = {};
+};
+StagedState g_staged[kMaxDevices];
+
+bool staged_setup(StagedState& r) {
+  if (r.ready) return true;
+  const unsigned sf = cudaStreamNonBlocking;
+  const unsigned ef = cudaEventDisableTiming;
+  if (cudaStreamCreateWithFlags(&r.up, sf) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&r.run, sf) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&r.down, sf) != cudaSuccess ||
+      cudaEventCreateWithFlags(&r.start, ef) != cudaSuccess ||
+      cudaEventCreateWithFlags(&r.done, ef) != cudaSuccess)
+    return false;
+  for (int c = 0; c < kMaxStagedChunks; ++c)
+    if (cudaEventCreateWithFlags(&r.uploaded[c], ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&r.computed[c], ef) != cudaSuccess)
+      return false;
+  r.ready = true;
+  return true;
+}
 
 bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -195,17 +230,50 @@ attn_status_t attn_fwd_staged(const void* q_h, const void* k_h, const void* v_h,
   attn_status_t s = validate(q_d, k_d, v_d, out_d, lse_d, B, H, S, D, scale, causal);
   if (s != ATTN_OK) return s;
   if (q_d == k_d || q_d == v_d || k_d == v_d) return ATTN_ERR_INVALID_ARG;
-  const size_t nt = static_cast<size_t>(B * H * S * D * 2);
-  const size_t nl = static_cast<size_t>(B * H * S * 4);
-  if (cudaMemcpyAsync(q_d, q_h, nt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(k_d, k_h, nt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(v_d, v_h, nt, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  s = launch(q_d, k_d, v_d, out_d, lse_d, B, H, S, D, scale, causal, false, kDefaultWaitTimeoutNs,
-             stream);
+  int dev = -1;
+  DeviceState* st = nullptr;
+  s = device_state(&dev, &st);
   if (s != ATTN_OK) return s;
-  if (cudaMemcpyAsync(out_h, out_d, nt, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-      cudaMemcpyAsync(lse_h, lse_d, nl, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  StagedState& r = g_staged[dev];
+  std::lock_guard<std::mutex> lock(r.mu);
+  if (!staged_setup(r)) return ATTN_ERR_CUDA;
+
+  // Chunks of (b, h) slices: chunk c's kernel overlaps chunk c+1's upload
+  // and chunk c-1's download.  Every stream starts after the work already on
+  // `stream`, and `stream` continues once the last download is done.
+  const int64_t BH = B * H;
+  const int64_t slice = S * D * 2;  // bytes of one slice of q, k, v or out
+  const int n = ea::staged_chunk_count(BH, 3 * slice, kStagedChunkBytes, kMaxStagedChunks);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaEventRecord(r.start, stream)) || !ok(cudaStreamWaitEvent(r.up, r.start, 0)) ||
+      !ok(cudaStreamWaitEvent(r.run, r.start, 0)) || !ok(cudaStreamWaitEvent(r.down, r.start, 0)))
+    return ATTN_ERR_CUDA;
+  const auto H2D = cudaMemcpyHostToDevice;
+  const auto D2H = cudaMemcpyDeviceToHost;
+  for (int c = 0; c < n; ++c) {
+    int64_t first = 0, count = 0;
+    ea::staged_chunk_range(BH, n, c, &first, &count);
+    const size_t off = static_cast<size_t>(first * slice), len = static_cast<size_t>(count * slice);
+    const size_t loff = static_cast<size_t>(first * S), llen = static_cast<size_t>(count * S * 4);
+    auto dptr = [off](void* p) { return static_cast<char*>(p) + off; };
+    auto hptr = [off](const void* p) { return static_cast<const char*>(p) + off; };
+    if (!ok(cudaMemcpyAsync(dptr(q_d), hptr(q_h), len, H2D, r.up)) ||
+        !ok(cudaMemcpyAsync(dptr(k_d), hptr(k_h), len, H2D, r.up)) ||
+        !ok(cudaMemcpyAsync(dptr(v_d), hptr(v_h), len, H2D, r.up)) ||
+        !ok(cudaEventRecord(r.uploaded[c], r.up)) ||
+        !ok(cudaStreamWaitEvent(r.run, r.uploaded[c], 0)))
+      return ATTN_ERR_CUDA;
+    s = ea::launch_with_status(dptr(q_d), dptr(k_d), dptr(v_d), dptr(out_d), lse_d + loff, 1,
+                               count, S, D, scale, causal, false, kDefaultWaitTimeoutNs,
+                               st->status, r.run);
+    if (s != ATTN_OK) return s;
+    if (!ok(cudaEventRecord(r.computed[c], r.run)) ||
+        !ok(cudaStreamWaitEvent(r.down, r.computed[c], 0)) ||
+        !ok(cudaMemcpyAsync(static_cast<char*>(out_h) + off, dptr(out_d), len, D2H, r.down)) ||
+        !ok(cudaMemcpyAsync(lse_h + loff, lse_d + loff, llen, D2H, r.down)))
+      return ATTN_ERR_CUDA;
+  }
+  if (!ok(cudaEventRecord(r.done, r.down)) || !ok(cudaStreamWaitEvent(stream, r.done, 0)))
     return ATTN_ERR_CUDA;
   return ATTN_OK;
 }

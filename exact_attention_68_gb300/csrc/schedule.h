@@ -79,4 +79,24 @@ inline UnitSchedule plan_schedule(int64_t BH, int64_t n_units, int64_t S, int64_
   return s;
 }
 
+// Host: how the staged (host-buffer) entry point splits the B·H slices into
+// chunks whose host↔device copies and kernels overlap.  About `target_bytes`
+// of inputs per chunk, at least one slice per chunk, at most `max_chunks`.
+inline int staged_chunk_count(int64_t BH, int64_t in_bytes_per_slice, int64_t target_bytes,
+                              int max_chunks) {
+  int64_t n = (BH * in_bytes_per_slice + target_bytes - 1) / target_bytes;
+  if (n > max_chunks) n = max_chunks;
+  if (n > BH) n = BH;
+  if (n < 1) n = 1;
+  return static_cast<int>(n);
+}
+
+// Slices [*first, *first + *count) of chunk c of n: the slices are spread
+// evenly, the first BH % n chunks taking one more.
+inline void staged_chunk_range(int64_t BH, int n, int c, int64_t* first, int64_t* count) {
+  const int64_t base = BH / n, rem = BH % n;
+  *count = base + (c < rem ? 1 : 0);
+  *first = c * base + (c < rem ? c : rem);
+}
+
 }  // namespace ea

@@ -95,12 +95,18 @@ ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, voi
  * attn_fwd_staged — the same forward, fed from and returned to HOST memory.
  *
  * q_h, k_h, v_h (bf16 [B,H,S,D]) are copied host→device into the caller's
- * device buffers q_d, k_d, v_d; attn_fwd runs on them writing out_d, lse_d;
+ * device buffers q_d, k_d, v_d; the forward runs on them writing out_d, lse_d;
  * out_d and lse_d are copied back to out_h (bf16 [B,H,S,D]) and lse_h (fp32
- * [B,H,S]).  All copies are cudaMemcpyAsync on `stream`; pass page-locked
- * host memory for them to be asynchronous.  Returns after enqueueing; the
- * host results are valid once the stream is synchronised.  Same argument
+ * [B,H,S]).  The (b, h) slices are split into chunks (about 48 MB of inputs
+ * each, at most 8) whose uploads, kernels and downloads overlap on three
+ * streams the library keeps per device; that work starts after everything
+ * already enqueued on `stream`, and `stream` waits for all of it, so the call
+ * behaves as one stream-ordered operation on `stream`.  Pass page-locked host
+ * memory for the copies to be asynchronous.  Returns after enqueueing; the
+ * host results are valid once the stream is synchronised, and the host and
+ * device buffers must not be touched by other work until then.  Same argument
  * rules as attn_fwd for the device side; host pointers must be non-NULL.
+ * Staged calls on one device are enqueued one at a time (a lock).
  */
 ATTN_API attn_status_t attn_fwd_staged(const void* q_h, const void* k_h, const void* v_h,
                               void* out_h, float* lse_h,

@@ -22,4 +22,14 @@ __attribute__((visibility("default"))) void sched_plan(int64_t BH, int64_t n_uni
   out[0] = s.heads_per_group;
   out[1] = s.tail_levels;
 }
+
+// The staged entry point's chunk plan: out[c] = {first, count} for c < n;
+// returns n.
+__attribute__((visibility("default"))) int staged_plan(int64_t BH, int64_t in_bytes_per_slice,
+                                                       int64_t target_bytes, int max_chunks,
+                                                       int64_t* out) {
+  const int n = ea::staged_chunk_count(BH, in_bytes_per_slice, target_bytes, max_chunks);
+  for (int c = 0; c < n; ++c) ea::staged_chunk_range(BH, n, c, out + 2 * c, out + 2 * c + 1);
+  return n;
+}
 }

@@ -156,6 +156,38 @@ def test_staged_host_entry_point_matches(cuda_device):
     assert torch.equal(out_h, ref_out) and torch.equal(lse_h, ref_lse)
 
 
+@pytest.mark.parametrize("shape", [(2, 9, 8192, 128), (1, 13, 16384, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_staged_chunked_pipeline_is_bitwise_the_device_path(cuda_device, shape):
+    """Inputs large enough that the staged call splits the slices into chunks
+    (18 slices into 3 even chunks; 13 into 7 + 6) whose copies and kernels
+    overlap on internal streams; two calls back to back on the same buffers,
+    each followed by a kernel on the caller's stream that reads the device
+    output, must see that call's own result."""
+    scale = default_scale(shape[3])
+    dev = torch.device("cuda:0")
+    q1, k1, v1 = make_qkv(shape, seed=14)
+    q2, k2, v2 = make_qkv(shape, seed=15)
+    refs = [run_gpu(q, k, v, scale, True) for q, k, v in ((q1, k1, v1), (q2, k2, v2))]
+    hosts = [tuple(x.pin_memory() for x in t) for t in ((q1, k1, v1), (q2, k2, v2))]
+    outs = [torch.empty_like(q1).pin_memory() for _ in range(2)]
+    lses = [torch.empty(shape[:3], dtype=torch.float32).pin_memory() for _ in range(2)]
+    qd, kd, vd = (torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    od = torch.empty_like(qd)
+    ld = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+    sums = []
+    for n in range(2):
+        binding.attn_fwd_staged(*hosts[n], outs[n], lses[n], qd, kd, vd, od, ld, scale=scale,
+                                causal=True)
+        sums.append(od.float().sum())  # a kernel on the caller's stream after the call
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.ATTN_OK
+    for n in range(2):
+        assert torch.equal(outs[n], refs[n][0]) and torch.equal(lses[n], refs[n][1])
+        # the same reduction on the GPU over the reference output: bitwise equal
+        assert sums[n].item() == refs[n][0].to(dev).float().sum().item()
+
+
 def test_binding_rejects_wrong_dtype_and_layout(cuda_device):
     q, k, v = (x.to("cuda:0") for x in make_qkv((1, 1, 128, 64)))
     with pytest.raises(TypeError):

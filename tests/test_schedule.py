@@ -111,3 +111,24 @@ def test_plan_long_context_causal(shim):
     assert _plan(shim, 32, 64, 16384, 128, True) == (6, 25)
     # B=2, H=16, S=4096, D=128: 2 MiB per slice -> 24 per group, 13 tail levels
     assert _plan(shim, 32, 16, 4096, 128, True) == (24, 13)
+
+
+@pytest.mark.parametrize("BH", [1, 2, 7, 13, 18, 32, 100])
+@pytest.mark.parametrize("per_slice_mb", [1, 6, 12, 48, 200])
+def test_staged_chunk_plan_covers_every_slice_once(shim, BH, per_slice_mb):
+    shim.staged_plan.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                 ctypes.POINTER(ctypes.c_int64)]
+    shim.staged_plan.restype = ctypes.c_int
+    out = (ctypes.c_int64 * 32)()
+    target, max_chunks = 48 << 20, 8
+    n = shim.staged_plan(BH, per_slice_mb << 20, target, max_chunks, out)
+    assert 1 <= n <= min(BH, max_chunks)
+    first = [out[2 * c] for c in range(n)]
+    count = [out[2 * c + 1] for c in range(n)]
+    assert first[0] == 0 and all(x >= 1 for x in count)
+    assert all(first[c] + count[c] == first[c + 1] for c in range(n - 1))
+    assert first[-1] + count[-1] == BH
+    assert max(count) - min(count) <= 1
+    # as many chunks as the inputs need at about `target` bytes each, capped
+    want = -(-BH * (per_slice_mb << 20) // target)
+    assert n == max(1, min(want, BH, max_chunks))
