@@ -555,16 +555,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
                                                 kSiteKvElemS | (g << 7) | (it & 0x7f)));
       if (!ok) break;
       tc_fence_after_sync();
-      uint32_t s[2][32], dp[2][32];
-      tmem_ld_32x32b_x32(tS, s[0]);
-      tmem_ld_32x32b_x32(tS + 32, s[1]);
-      tmem_ld_32x32b_x32(tP, dp[0]);
-      tmem_ld_32x32b_x32(tP + 32, dp[1]);
-      tmem_ld_wait();
-      reg_fence(s[0]);
-      reg_fence(s[1]);
-      reg_fence(dp[0]);
-      reg_fence(dp[1]);
       // allowed query columns of this half: lo .. hi (causal: query >= key; query < S)
       const int c0 = i * kTileRows + 64 * g;
       const int hi = p.S - 1 - c0;
@@ -574,25 +564,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       // (lse·log2e, delta) of this half's 64 query columns, two columns per load
       const float4* stat = reinterpret_cast<const float4*>(
           smem_gen + L::kStatOff + st * L::kStatBytes + 8 * 64 * g);
-      uint32_t ppk[32], dpk[32];
+      // Two passes of 32 columns keep the live registers down; pass 1 writes
+      // its packed results over columns 16-31, which pass 0 has already read.
 #pragma unroll
-      for (int e2 = 0; e2 < 32; ++e2) {
-        const int h = e2 >> 4;
-        const int e = (2 * e2) & 31;
-        const float4 sd = stat[e2];  // lse2[c], delta[c], lse2[c+1], delta[c+1]
-        float p0 = ex2_approx(fmaf(__uint_as_float(s[h][e]), sl2, -sd.x));
-        float p1 = ex2_approx(fmaf(__uint_as_float(s[h][e + 1]), sl2, -sd.z));
-        if (edge) {
-          if (2 * e2 < lo || 2 * e2 > hi) p0 = 0.f;
-          if (2 * e2 + 1 < lo || 2 * e2 + 1 > hi) p1 = 0.f;
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t s[32], dp[32];
+        tmem_ld_32x32b_x32(tS + 32 * pass, s);
+        tmem_ld_32x32b_x32(tP + 32 * pass, dp);
+        tmem_ld_wait();
+        reg_fence(s);
+        reg_fence(dp);
+        uint32_t ppk[16], dpk[16];
+#pragma unroll
+        for (int e2 = 0; e2 < 16; ++e2) {
+          const int c = 32 * pass + 2 * e2;  // column within the half
+          const float4 sd = stat[16 * pass + e2];  // lse2[c], delta[c], lse2[c+1], delta[c+1]
+          float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * e2]), sl2, -sd.x));
+          float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * e2 + 1]), sl2, -sd.z));
+          if (edge) {
+            if (c < lo || c > hi) p0 = 0.f;
+            if (c + 1 < lo || c + 1 > hi) p1 = 0.f;
+          }
+          const float ds0 = p0 * (__uint_as_float(dp[2 * e2]) - sd.y);
+          const float ds1 = p1 * (__uint_as_float(dp[2 * e2 + 1]) - sd.w);
+          ppk[e2] = pack_x2<F16>(p0, p1);
+          dpk[e2] = pack_x2<F16>(ds0, ds1);
         }
-        const float ds0 = p0 * (__uint_as_float(dp[h][e]) - sd.y);
-        const float ds1 = p1 * (__uint_as_float(dp[h][e + 1]) - sd.w);
-        ppk[e2] = pack_x2<F16>(p0, p1);
-        dpk[e2] = pack_x2<F16>(ds0, ds1);
+        tmem_st_32x32b_x16(tS + 16 * pass, ppk);
+        tmem_st_32x32b_x16(tP + 16 * pass, dpk);
       }
-      tmem_st_32x32b_x32(tS, ppk);
-      tmem_st_32x32b_x32(tP, dpk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kPFull + g));
