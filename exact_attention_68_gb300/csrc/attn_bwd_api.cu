@@ -76,6 +76,7 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
       !ea::encode_bhsd_16bit(&p.tm_dk, dk, BH, S, D, 32, f16) ||
       !ea::encode_bhsd_16bit(&p.tm_dv, dv, BH, S, D, 32, f16))
     return ATTN_ERR_CUDA;
+  p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<const uint16_t*>(out);
   p.dout = static_cast<const uint16_t*>(dout);
   p.lse = lse;

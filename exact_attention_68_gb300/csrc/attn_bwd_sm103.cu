@@ -140,15 +140,13 @@ template <int D>
 struct DqLayout {
   static constexpr int kTile = kTileRows * D * 2;
   static constexpr int kChunks = D / 64;
-  static constexpr int kKStages = (D == 128) ? 3 : 4;  // K ring depth
-  static constexpr int kVStages = (D == 128) ? 2 : 3;  // V ring depth (V is released earlier)
-  static constexpr int kQOff = 0;
-  static constexpr int kDoOff = kTile;
-  static constexpr int kKOff = 2 * kTile;
+  static constexpr int kKStages = (D == 128) ? 4 : 6;  // K ring depth
+  static constexpr int kVStages = (D == 128) ? 3 : 5;  // V ring depth (V is released earlier)
+  static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKStages * kTile;
   static constexpr int kPartOff = kVOff + kVStages * kTile;  // float [2][128] delta halves
   static constexpr int kBarOff = kPartOff + 2 * kTileRows * 4;
-  static constexpr int kQFull = 0;                   // Q and dO landed
+  static constexpr int kQFull = 0;                   // Q and dO in TMEM (256 arrivals)
   static constexpr int kKFull = 1;                   // [kKStages]
   static constexpr int kKEmpty = kKFull + kKStages;  // [kKStages]
   static constexpr int kVFull = kKEmpty + kKStages;  // [kVStages]
@@ -162,6 +160,11 @@ struct DqLayout {
   static constexpr int kAlloc = kMiscOff + 16 + 1024;
   static_assert(kAlloc <= 232448, "shared memory budget exceeded");
   static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns of Q and dO as the A operand of S and dP (two 16-bit values
+  // per column): after the two S/dP buffers and dQ
+  static constexpr uint32_t kQCol = 384;
+  static constexpr uint32_t kDoCol = 384 + D / 2;
+  static_assert(kDoCol + D / 2 <= kTmemCols, "TMEM budget exceeded");
 };
 
 template <int D, bool CAUSAL, bool F16>
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
   const int nkv = CAUSAL ? i + 1 : p.n_t;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::kQFull), 1);
+    mbar_init(bar(L::kQFull), 256);
 #pragma unroll
     for (int s = 0; s < L::kKStages; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
@@ -225,14 +228,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     const uint32_t tP = tS + 64;
     const uint32_t tQ = tmem_base + lane_bits + 256;
 
-    // delta = rowsum(dout ⊙ out): each warpgroup sums half of the row
+    // Each warpgroup takes half of its row's D columns: it puts that half of
+    // the Q and dO rows into TMEM (the A operand of S and dP for the whole
+    // loop, so shared memory only feeds the K/V side) and sums that half of
+    // delta = rowsum(dout ⊙ out).
     float part = 0.f;
-    if (valid) {
-      const int64_t base = ((int64_t)bh * p.S + grow) * D;
-      const uint4* o4 = reinterpret_cast<const uint4*>(p.out + base) + g * (D / 16);
-      const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + base) + g * (D / 16);
+    {
+      constexpr int kU = D / 16;  // 16-byte groups in half a row
+      uint32_t qw[4 * kU], dw[4 * kU];
+      if (valid) {
+        const int64_t base = ((int64_t)bh * p.S + grow) * D;
+        const uint4* q4 = reinterpret_cast<const uint4*>(p.q + base) + g * kU;
+        const uint4* o4 = reinterpret_cast<const uint4*>(p.out + base) + g * kU;
+        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + base) + g * kU;
 #pragma unroll
-      for (int u = 0; u < D / 16; ++u) part += dot8<F16>(__ldg(o4 + u), __ldg(d4 + u));
+        for (int u = 0; u < kU; ++u) {
+          const uint4 qv = __ldg(q4 + u), dv = __ldg(d4 + u);
+          part += dot8<F16>(__ldg(o4 + u), dv);
+          qw[4 * u] = qv.x, qw[4 * u + 1] = qv.y, qw[4 * u + 2] = qv.z, qw[4 * u + 3] = qv.w;
+          dw[4 * u] = dv.x, dw[4 * u + 1] = dv.y, dw[4 * u + 2] = dv.z, dw[4 * u + 3] = dv.w;
+        }
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4 * kU; ++w) qw[w] = dw[w] = 0u;
+      }
+      tmem_st_words(tmem_base + lane_bits + L::kQCol + g * (D / 4), qw);
+      tmem_st_words(tmem_base + lane_bits + L::kDoCol + g * (D / 4), dw);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kQFull));
     }
     st_shared_f32(sb + L::kPartOff + 4 * (g * kTileRows + row), part);
     named_bar_sync(1, 256);
@@ -285,14 +309,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       mbar_arrive(bar(L::kPFull + g));
     }
 
-    // ---- epilogue: dQ · scale → bf16 → swizzled staging (Q's buffer) → TMA store
+    // ---- epilogue: dQ · scale → 16-bit → swizzled staging (K stage 0, idle
+    // once every MMA has completed) → TMA store
     if (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kOFull), 0, ctl, kSiteDqElemO));
     }
     if (ok) {
       tc_fence_after_sync();
       for (int c = g; c < L::kChunks; c += 2)
-        store_chunk<F16>(tQ + c * 64, sb + L::kQOff + c * kChunkBytes, row, p.scale, &p.tm_dq, c * 64,
+        store_chunk<F16>(tQ + c * 64, sb + L::kKOff + c * kChunkBytes, row, p.scale, &p.tm_dq, c * 64,
                     i * kTileRows, bh, wq, lane);
       if (lane == 0) {
         tma_store_commit();
@@ -303,21 +328,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
   } else if (warp == 9) {
     // ======================= TMA producer =======================
     if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_do);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_dq);
-      const uint64_t pol_once = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      mbar_arrive_expect_tx(bar(L::kQFull), 2 * L::kTile);
-#pragma unroll
-      for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_3d(sb + L::kQOff + c * kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64,
-                    i * kTileRows, bh, pol_once);
-        tma_load_3d(sb + L::kDoOff + c * kChunkBytes, &p.tm_do, bar(L::kQFull), c * 64,
-                    i * kTileRows, bh, pol_once);
-      }
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int j = 0; j < nkv; ++j) {
@@ -352,7 +366,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
                             kSiteDqProducer | 0xff);
       }
       if (!ok) {
-        wait_drain(bar(L::kQFull), 0, kDrainLimitNs);
         for (int j = max(k_issued - L::kKStages, 0); j < k_issued; ++j)
           wait_drain(bar(L::kKFull + j % L::kKStages), (j / L::kKStages) & 1, kDrainLimitNs);
         for (int j = max(v_issued - L::kVStages, 0); j < v_issued; ++j)
@@ -366,27 +379,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     constexpr uint32_t kIdescQ = instr_desc_16bit(kTileRows, D, false, true, F16);
     constexpr uint32_t kTileUnits = L::kTile >> 4;
     constexpr uint32_t kHalfUnits = (64 * 128) >> 4;  // 64 rows of a 128-byte-row block
-    const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
-    const uint64_t ddo = smem_desc_sw128(sb + L::kDoOff, 16, 1024);
     const uint64_t dk = smem_desc_sw128(sb + L::kKOff, 16, 1024);
     const uint64_t dv = smem_desc_sw128(sb + L::kVOff, 16, 1024);
     const uint64_t dk_mn = smem_desc_sw128(sb + L::kKOff, kChunkBytes, 1024);
     auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
       return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
     };
-    // SP(j, h): S_h = Q · K_j[64h, 64h+64)ᵀ and dP_h = dO · V_j[64h, 64h+64)ᵀ
+    // SP(j, h): S_h = Q · K_j[64h, 64h+64)ᵀ and dP_h = dO · V_j[64h, 64h+64)ᵀ,
+    // A (Q, dO) from TMEM, 8 columns per K step of 16
     auto issue_sp = [&](int ks, int vs, int h) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ss(tmem_base + 128 * h, dq + off, dk + ks * kTileUnits + h * kHalfUnits + off,
-               kIdescSP, kk > 0 ? 1u : 0u);
+        mma_ts(tmem_base + 128 * h, tmem_base + L::kQCol + kk * 8,
+               dk + ks * kTileUnits + h * kHalfUnits + off, kIdescSP, kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ss(tmem_base + 128 * h + 64, ddo + off, dv + vs * kTileUnits + h * kHalfUnits + off,
-               kIdescSP, kk > 0 ? 1u : 0u);
+        mma_ts(tmem_base + 128 * h + 64, tmem_base + L::kDoCol + kk * 8,
+               dv + vs * kTileUnits + h * kHalfUnits + off, kIdescSP, kk > 0 ? 1u : 0u);
       }
       mma_commit(bar(L::kSFull + h));
     };
