@@ -22,6 +22,8 @@ struct BwdParams {
   CUtensorMap tm_dk;  // dk, same
   CUtensorMap tm_dv;  // dv, same
   const uint16_t* q;     // 16-bit [B·H, S, D]: rows read into TMEM by the dq kernel
+  const uint16_t* k;     // 16-bit [B·H, S, D]: rows read into TMEM by the dk/dv kernel
+  const uint16_t* v;     // 16-bit [B·H, S, D]: rows read into TMEM by the dk/dv kernel
   const uint16_t* out;   // 16-bit [B·H, S, D]: forward output (rows read for delta)
   const uint16_t* dout;  // 16-bit [B·H, S, D]
   const float* lse;      // [B·H, S]: natural-log logsumexp saved by the forward

@@ -77,6 +77,8 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
       !ea::encode_bhsd_16bit(&p.tm_dv, dv, BH, S, D, 32, f16))
     return ATTN_ERR_CUDA;
   p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
   p.out = static_cast<const uint16_t*>(out);
   p.dout = static_cast<const uint16_t*>(dout);
   p.lse = lse;

@@ -475,24 +475,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
 }
 
 // ============================================================== dk/dv kernel
+//
+// K_j and V_j are the A operand of every Sᵀ / dPᵀ product of the CTA, so they
+// are put into TMEM once; shared memory then only feeds Q and dO.  Each Q tile
+// is taken as four 32-column quarters ("sub-steps" t = 4·it + q) in two TMEM
+// buffers; warpgroup b takes the sub-steps with t ≡ b (mod 2), i.e. quarters
+// b and b+2 of every tile.  TMEM columns (D = 128):
+//   buffer b: Sᵀ [64b, 64b+32), dPᵀ [64b+32, 64b+64)
+//   K [128, 128+D/2), V [128+D/2, 128+D)   (two 16-bit values per column)
+//   dV [256, 256+D), dK [256+D, 256+2D)
 
 template <int D>
 struct KvLayout {
   static constexpr int kTile = kTileRows * D * 2;
   static constexpr int kChunks = D / 64;
-  static constexpr int kStages = (D == 128) ? 2 : 3;  // Q/dO ring depth
+  static constexpr int kStages = (D == 128) ? 3 : 4;  // Q/dO ring depth
   static constexpr int kStatBytes = 2 * kTileRows * 4;  // (lse·log2e, delta) per query row
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kTile;
-  static constexpr int kQOff = 2 * kTile;
+  static constexpr int kQOff = 0;
   static constexpr int kDoOff = kQOff + kStages * kTile;
   static constexpr int kStatOff = kDoOff + kStages * kTile;
   static constexpr int kBarOff = kStatOff + kStages * kStatBytes;
-  static constexpr int kKVFull = 0;                 // K_j and V_j landed
+  static constexpr int kKVTmem = 0;                 // K_j, V_j in TMEM (256 arrivals)
   static constexpr int kFull = 1;                   // [kStages] Q_i, dO_i, stats landed
   static constexpr int kEmpty = kFull + kStages;    // [kStages]
-  static constexpr int kSFull = kEmpty + kStages;   // [2] Sᵀ_h and dPᵀ_h computed
-  static constexpr int kPFull = kSFull + 2;         // [2] Pᵀ_h and dSᵀ_h stored (128 arrivals)
+  static constexpr int kSFull = kEmpty + kStages;   // [2] Sᵀ and dPᵀ of buffer b computed
+  static constexpr int kPFull = kSFull + 2;         // [2] Pᵀ and dSᵀ of buffer b stored (128)
   static constexpr int kOFull = kPFull + 2;         // dK, dV final
   static constexpr int kDrain = kOFull + 1;
   static constexpr int kNumBars = kDrain + 1;
@@ -500,7 +507,12 @@ struct KvLayout {
   static constexpr int kAlloc = kMiscOff + 16 + 1024;
   static_assert(kAlloc <= 232448, "shared memory budget exceeded");
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(256 + 2 * D <= 512, "TMEM budget exceeded");
+  static constexpr uint32_t kKCol = 128;
+  static constexpr uint32_t kVCol = 128 + D / 2;
+  static constexpr uint32_t kDvCol = 256;
+  static constexpr uint32_t kDkCol = 256 + D;
+  static_assert(kDkCol + D <= kTmemCols, "TMEM budget exceeded");
+  static_assert(2 * kTile <= kStages * kTile, "dK/dV staging must fit the Q ring");
 };
 
 template <int D, bool CAUSAL, bool F16>
@@ -521,18 +533,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   const int bh = blockIdx.x - j * p.BH;
   const int i0 = CAUSAL ? j : 0;
   const int nq = p.n_t - i0;
+  const int n_sub = 4 * nq;  // quarter sub-steps
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::kKVFull), 1);
+    mbar_init(bar(L::kKVTmem), 256);
 #pragma unroll
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kFull + s), 1);
       mbar_init(bar(L::kEmpty + s), 1);
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(bar(L::kSFull + h), 1);
-      mbar_init(bar(L::kPFull + h), 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::kSFull + b), 1);
+      mbar_init(bar(L::kPFull + b), 128);
     }
     mbar_init(bar(L::kOFull), 1);
     mbar_init(bar(L::kDrain), 1);
@@ -550,80 +563,102 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
 
   if (warp < 8) {
-    // ======================= elementwise: Pᵀ, dSᵀ, epilogue =======================
-    const int g = warp >> 2;            // half of every Q tile this warpgroup takes
+    // ======================= elementwise: K/V to TMEM, Pᵀ, dSᵀ, epilogue =======================
+    const int g = warp >> 2;            // TMEM buffer (quarters g and g+2) of this warpgroup
     const int wq = warp & 3;
     const int r = wq * 32 + lane;       // key row within the tile (TMEM lane)
     const int gk = j * kTileRows + r;   // key row in the sequence
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem_base + lane_bits + 128 * g;
-    const uint32_t tP = tS + 64;
+    const uint32_t tS = tmem_base + lane_bits + 64 * g;
+    const uint32_t tP = tS + 32;
     const float sl2 = p.scale_log2;
+    {
+      // this row's K and V, half of D per warpgroup, into TMEM (rows past the end: 0)
+      constexpr int kU = D / 16;  // 16-byte groups in half a row
+      uint32_t kw[4 * kU], vw[4 * kU];
+      if (gk < p.S) {
+        const int64_t base = ((int64_t)bh * p.S + gk) * D;
+        const uint4* k4 = reinterpret_cast<const uint4*>(p.k + base) + g * kU;
+        const uint4* v4 = reinterpret_cast<const uint4*>(p.v + base) + g * kU;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const uint4 kv = __ldg(k4 + u), vv = __ldg(v4 + u);
+          kw[4 * u] = kv.x, kw[4 * u + 1] = kv.y, kw[4 * u + 2] = kv.z, kw[4 * u + 3] = kv.w;
+          vw[4 * u] = vv.x, vw[4 * u + 1] = vv.y, vw[4 * u + 2] = vv.z, vw[4 * u + 3] = vv.w;
+        }
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4 * kU; ++w) kw[w] = vw[w] = 0u;
+      }
+      tmem_st_words(tmem_base + lane_bits + L::kKCol + g * (D / 4), kw);
+      tmem_st_words(tmem_base + lane_bits + L::kVCol + g * (D / 4), vw);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kKVTmem));
+    }
     bool ok = true;
-    for (int it = 0; it < nq; ++it) {
+    for (int t = g; t < n_sub; t += 2) {
+      const int it = t >> 2;
+      const int q = t & 3;
       const int i = i0 + it;
       const int st = it % L::kStages;
-      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kSFull + g), it & 1, ctl,
-                                                kSiteKvElemS | (g << 7) | (it & 0x7f)));
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kSFull + g), (t >> 1) & 1, ctl,
+                                                kSiteKvElemS | (g << 7) | (t & 0x7f)));
       if (!ok) break;
       tc_fence_after_sync();
-      // allowed query columns of this half: lo .. hi (causal: query >= key; query < S)
-      const int c0 = i * kTileRows + 64 * g;
+      uint32_t s[32], dp[32];
+      tmem_ld_32x32b_x32(tS, s);
+      tmem_ld_32x32b_x32(tP, dp);
+      tmem_ld_wait();
+      reg_fence(s);
+      reg_fence(dp);
+      // allowed query columns of this quarter: lo .. hi (causal: query >= key; query < S)
+      const int c0 = i * kTileRows + 32 * q;
       const int hi = p.S - 1 - c0;
       int lo = CAUSAL ? gk - c0 : 0;
-      if (gk >= p.S) lo = 64;  // key row past the end: nothing
-      const bool edge = lo > 0 || hi < 63;
-      // (lse·log2e, delta) of this half's 64 query columns, two columns per load
+      if (gk >= p.S) lo = 32;  // key row past the end: nothing
+      const bool edge = lo > 0 || hi < 31;
+      // (lse·log2e, delta) of this quarter's 32 query columns, two columns per load
       const float4* stat = reinterpret_cast<const float4*>(
-          smem_gen + L::kStatOff + st * L::kStatBytes + 8 * 64 * g);
-      // Two passes of 32 columns keep the live registers down; pass 1 writes
-      // its packed results over columns 16-31, which pass 0 has already read.
+          smem_gen + L::kStatOff + st * L::kStatBytes + 8 * 32 * q);
+      uint32_t ppk[16], dpk[16];
 #pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {
-        uint32_t s[32], dp[32];
-        tmem_ld_32x32b_x32(tS + 32 * pass, s);
-        tmem_ld_32x32b_x32(tP + 32 * pass, dp);
-        tmem_ld_wait();
-        reg_fence(s);
-        reg_fence(dp);
-        uint32_t ppk[16], dpk[16];
-#pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          const int c = 32 * pass + 2 * e2;  // column within the half
-          const float4 sd = stat[16 * pass + e2];  // lse2[c], delta[c], lse2[c+1], delta[c+1]
-          float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * e2]), sl2, -sd.x));
-          float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * e2 + 1]), sl2, -sd.z));
-          if (edge) {
-            if (c < lo || c > hi) p0 = 0.f;
-            if (c + 1 < lo || c + 1 > hi) p1 = 0.f;
-          }
-          const float ds0 = p0 * (__uint_as_float(dp[2 * e2]) - sd.y);
-          const float ds1 = p1 * (__uint_as_float(dp[2 * e2 + 1]) - sd.w);
-          ppk[e2] = pack_x2<F16>(p0, p1);
-          dpk[e2] = pack_x2<F16>(ds0, ds1);
+      for (int e2 = 0; e2 < 16; ++e2) {
+        const int c = 2 * e2;
+        const float4 sd = stat[e2];  // lse2[c], delta[c], lse2[c+1], delta[c+1]
+        float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -sd.x));
+        float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, -sd.z));
+        if (edge) {
+          if (c < lo || c > hi) p0 = 0.f;
+          if (c + 1 < lo || c + 1 > hi) p1 = 0.f;
         }
-        tmem_st_32x32b_x16(tS + 16 * pass, ppk);
-        tmem_st_32x32b_x16(tP + 16 * pass, dpk);
+        const float ds0 = p0 * (__uint_as_float(dp[c]) - sd.y);
+        const float ds1 = p1 * (__uint_as_float(dp[c + 1]) - sd.w);
+        ppk[e2] = pack_x2<F16>(p0, p1);
+        dpk[e2] = pack_x2<F16>(ds0, ds1);
       }
+      tmem_st_32x32b_x16(tS, ppk);
+      tmem_st_32x32b_x16(tP, dpk);
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kPFull + g));
     }
 
-    // ---- epilogue: warpgroup 0 stores dV (staged in V_j's buffer), 1 stores dK · scale
+    // ---- epilogue: warpgroup 0 stores dV, 1 stores dK · scale, staged in the
+    // (idle once every MMA has completed) Q ring
     if (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kOFull), 0, ctl, kSiteKvElemO));
     }
     if (ok) {
       tc_fence_after_sync();
-      const uint32_t tAcc = tmem_base + lane_bits + 256 + g * D;
-      const uint32_t stage = sb + (g == 0 ? L::kVOff : L::kKOff);
+      const uint32_t tAcc = tmem_base + lane_bits + (g == 0 ? L::kDvCol : L::kDkCol);
+      const uint32_t stage = sb + L::kQOff + g * L::kTile;
       const CUtensorMap* map = g == 0 ? &p.tm_dv : &p.tm_dk;
       const float mul = g == 0 ? 1.f : p.scale;
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
-        store_chunk<F16>(tAcc + c * 64, stage + c * kChunkBytes, r, mul, map, c * 64, j * kTileRows, bh,
-                    wq, lane);
+        store_chunk<F16>(tAcc + c * 64, stage + c * kChunkBytes, r, mul, map, c * 64, j * kTileRows,
+                         bh, wq, lane);
       if (lane == 0) {
         tma_store_commit();
         tma_store_wait_all();
@@ -631,24 +666,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
     }
     tc_fence_before_sync();
   } else if (warp == 9) {
-    // ======================= producer: K_j, V_j once; Q_i, dO_i, stats per step =======================
-    const uint64_t pol_once = l2_policy_evict_first();
+    // ======================= producer: Q_i, dO_i, stats per Q tile =======================
     const uint64_t pol_q = l2_policy_evict_last();
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_do);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_dk);
       tma_prefetch_desc(&p.tm_dv);
-      mbar_arrive_expect_tx(bar(L::kKVFull), 2 * L::kTile);
-#pragma unroll
-      for (int c = 0; c < L::kChunks; ++c) {
-        tma_load_3d(sb + L::kKOff + c * kChunkBytes, &p.tm_k, bar(L::kKVFull), c * 64,
-                    j * kTileRows, bh, pol_once);
-        tma_load_3d(sb + L::kVOff + c * kChunkBytes, &p.tm_v, bar(L::kKVFull), c * 64,
-                    j * kTileRows, bh, pol_once);
-      }
     }
     const int64_t row0 = (int64_t)bh * p.S;
     int issued = 0;
@@ -690,7 +714,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
                             kSiteKvProducer | 0xff);
       }
       if (!ok) {
-        wait_drain(bar(L::kKVFull), 0, kDrainLimitNs);
         for (int it = max(issued - L::kStages, 0); it < issued; ++it)
           wait_drain(bar(L::kFull + it % L::kStages), (it / L::kStages) & 1, kDrainLimitNs);
       }
@@ -699,12 +722,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
     const bool leader = elect_one();
-    constexpr uint32_t kIdescSP = instr_desc_16bit(kTileRows, 64, false, false, F16);  // 64 queries
+    constexpr uint32_t kIdescSP = instr_desc_16bit(kTileRows, 32, false, false, F16);  // 32 queries
     constexpr uint32_t kIdescG = instr_desc_16bit(kTileRows, D, false, true, F16);
     constexpr uint32_t kTileUnits = L::kTile >> 4;
-    constexpr uint32_t kHalfUnits = (64 * 128) >> 4;  // 64 rows of a 128-byte-row block
-    const uint64_t dk = smem_desc_sw128(sb + L::kKOff, 16, 1024);
-    const uint64_t dv = smem_desc_sw128(sb + L::kVOff, 16, 1024);
+    constexpr uint32_t kQuarterUnits = (32 * 128) >> 4;  // 32 rows of a 128-byte-row block
     const uint64_t dq = smem_desc_sw128(sb + L::kQOff, 16, 1024);
     const uint64_t ddo = smem_desc_sw128(sb + L::kDoOff, 16, 1024);
     const uint64_t dq_mn = smem_desc_sw128(sb + L::kQOff, kChunkBytes, 1024);
@@ -712,67 +733,66 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
     auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
       return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
     };
-    // SP(it, h): Sᵀ_h = K_j · Q_i[64h, 64h+64)ᵀ and dPᵀ_h = V_j · dO_i[64h, 64h+64)ᵀ
-    auto issue_sp = [&](int st, int h) {
+    // SP(t): Sᵀ = K_j · Q_i[32q, 32q+32)ᵀ and dPᵀ = V_j · dO_i[32q, 32q+32)ᵀ into
+    // buffer t & 1; A (K, V) from TMEM, 8 columns per K step of 16
+    auto issue_sp = [&](int t) {
+      const int b = t & 1, q = t & 3, st = (t >> 2) % L::kStages;
+      const uint32_t bq = st * kTileUnits + q * kQuarterUnits;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ss(tmem_base + 128 * h, dk + off, dq + st * kTileUnits + h * kHalfUnits + off,
-               kIdescSP, kk > 0 ? 1u : 0u);
+        mma_ts(tmem_base + 64 * b, tmem_base + L::kKCol + kk * 8, dq + bq + off, kIdescSP,
+               kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ss(tmem_base + 128 * h + 64, dv + off, ddo + st * kTileUnits + h * kHalfUnits + off,
-               kIdescSP, kk > 0 ? 1u : 0u);
+        mma_ts(tmem_base + 64 * b + 32, tmem_base + L::kVCol + kk * 8, ddo + bq + off, kIdescSP,
+               kk > 0 ? 1u : 0u);
       }
-      mma_commit(bar(L::kSFull + h));
+      mma_commit(bar(L::kSFull + b));
     };
-    // G(it, h): dV += Pᵀ_h · dO_i[64h, 64h+64), dK += dSᵀ_h · Q_i[64h, 64h+64)
-    auto issue_g = [&](int st, int h, bool first) {
+    // G(t): dV += Pᵀ · dO_i[32q, 32q+32), dK += dSᵀ · Q_i[32q, 32q+32)
+    auto issue_g = [&](int t) {
+      const int b = t & 1, q = t & 3, st = (t >> 2) % L::kStages;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t a = 128 * h + kk * 8;
-        const uint32_t b = st * kTileUnits + (4 * h + kk) * (2048 >> 4);
-        const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-        mma_ts(tmem_base + 256, tmem_base + a, ddo_mn + b, kIdescG, acc);
-        mma_ts(tmem_base + 256 + D, tmem_base + a + 64, dq_mn + b, kIdescG, acc);
+      for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t a = 64 * b + kk * 8;
+        const uint32_t bo = st * kTileUnits + (2 * q + kk) * (2048 >> 4);
+        const uint32_t acc = (t == 0 && kk == 0) ? 0u : 1u;
+        mma_ts(tmem_base + L::kDvCol, tmem_base + a, ddo_mn + bo, kIdescG, acc);
+        mma_ts(tmem_base + L::kDkCol, tmem_base + a + 32, dq_mn + bo, kIdescG, acc);
       }
     };
 
-    bool ok = wait_warp(bar(L::kKVFull), 0, kSiteKvMmaKV);
+    bool ok = wait_warp(bar(L::kKVTmem), 0, kSiteKvMmaKV);
     if (ok) ok = wait_warp(bar(L::kFull + 0), 0, kSiteKvMmaQ);
     if (ok) {
       tc_fence_after_sync();
       if (leader) {
-        issue_sp(0, 0);
-        issue_sp(0, 1);
+        issue_sp(0);
+        issue_sp(1);
       }
       __syncwarp();
     }
-    for (int it = 0; it < nq && ok; ++it) {
-      const int st = it % L::kStages;
-      const bool more = it + 1 < nq;
-      const int stn = (it + 1) % L::kStages;
-      ok = wait_warp(bar(L::kPFull + 0), it & 1, kSiteKvMmaP | (it & 0x7f));
+    for (int t = 0; t < n_sub && ok; ++t) {
+      const int b = t & 1;
+      ok = wait_warp(bar(L::kPFull + b), (t >> 1) & 1, kSiteKvMmaP | (b << 7) | (t & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader) issue_g(st, 0, it == 0);
-      __syncwarp();
-      if (more) {
-        ok = wait_warp(bar(L::kFull + stn), ((it + 1) / L::kStages) & 1, kSiteKvMmaQ | (it & 0xff));
+      const int t2 = t + 2;
+      if ((t2 & 3) == 0 && t2 < n_sub) {
+        // the next sub-step opens Q tile t2 / 4: its stage must have landed
+        const int it2 = t2 >> 2;
+        ok = wait_warp(bar(L::kFull + it2 % L::kStages), (it2 / L::kStages) & 1,
+                       kSiteKvMmaQ | (it2 & 0xff));
         if (!ok) break;
         tc_fence_after_sync();
-        if (leader) issue_sp(stn, 0);
-        __syncwarp();
       }
-      ok = wait_warp(bar(L::kPFull + 1), it & 1, kSiteKvMmaP | 0x80 | (it & 0x7f));
-      if (!ok) break;
-      tc_fence_after_sync();
       if (leader) {
-        issue_g(st, 1, false);
-        mma_commit(bar(L::kEmpty + st));  // Q_i, dO_i: last read by G(it, 1)
-        if (more) issue_sp(stn, 1);
+        issue_g(t);
+        if ((t & 3) == 3) mma_commit(bar(L::kEmpty + (t >> 2) % L::kStages));  // Q_i, dO_i done
+        if (t2 < n_sub) issue_sp(t2);
       }
       __syncwarp();
     }
