@@ -196,3 +196,21 @@ def test_binding_rejects_wrong_dtype_and_layout(cuda_device):
         binding.attn_fwd(q.transpose(1, 2), k, v)
     with pytest.raises(binding.AttnError):
         binding.attn_fwd(q, k, v, scale=-1.0)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_long_context_131072(cuda_device, D):
+    """The longest context here: S = 131072 (1024 Q tiles, 512 units of the
+    causal triangle per slice).  Rows 0, 1, 127, 128, S/2, S-129, S-1 and 48
+    rows from default_rng(7) of each of the two heads against the oracle."""
+    B, H, S = 1, 2, 131072
+    q, k, v = make_qkv((B, H, S, D), seed=16)
+    scale = default_scale(D)
+    out, lse = run_gpu(q, k, v, scale, True)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, S // 2, S - 129, S - 1], rng.integers(0, S, 48)]))
+    idx = np.asarray([(0, h, int(i)) for h in range(H) for i in rows], dtype=np.int64)
+    ro, rl = _oracle_rows(q, k, v, scale, True, idx)
+    og = to_f64(out)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    lg = to_f64(lse)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    compare(og, lg, ro, rl, f"S=131072 D={D}")

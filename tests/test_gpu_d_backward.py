@@ -153,3 +153,22 @@ def test_bwd_causal_grads_of_last_key_come_from_last_query_only(cuda_device):
     _, dk1, dv1, _ = _run_bwd(q, k, v, out, lse, d1, scale, True)
     _, dk2, dv2, _ = _run_bwd(q, k, v, out, lse, d2, scale, True)
     assert torch.equal(dk1[:, :, -1], dk2[:, :, -1]) and torch.equal(dv1[:, :, -1], dv2[:, :, -1])
+
+
+def test_bwd_long_context_32768(cuda_device):
+    """S = 32768, one head: 256 K/V tiles per dq CTA and 256 Q tiles per dk/dv
+    CTA; 160 sampled rows of dq, dk, dv against the oracle's row form."""
+    shape = (1, 1, 32768, 128)
+    q, k, v = make_qkv(shape, seed=71)
+    dout = _dout(shape, 72)
+    scale = default_scale(128)
+    out, lse = run_gpu(q, k, v, scale, True)
+    dq, dk, dv, _ = _run_bwd(q, k, v, out, lse, dout, scale, True)
+    n = [x.float().numpy() for x in (q, k, v, dout)]
+    rng = np.random.default_rng(73)
+    rows = np.unique(np.concatenate([[0, 127, 128, 32767 - 128, 32767], rng.integers(0, 32768, 155)]))
+    rq, rk, rv = attention_bwd_rows(*n, scale, True, 0, 0, rows, rows)
+    Mq, Mk, Mv = bwd_magnitudes(*n, scale, True, 0, 0, rows, rows)
+    compare_grad(to_f64(dq)[0, 0, rows], rq, Mq, "S=32768 dq")
+    compare_grad(to_f64(dk)[0, 0, rows], rk, Mk, "S=32768 dk")
+    compare_grad(to_f64(dv)[0, 0, rows], rv, Mv, "S=32768 dv")
