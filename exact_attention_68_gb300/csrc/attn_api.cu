@@ -16,10 +16,7 @@
 
 namespace {
 
-constexpr uint64_t kDefaultWaitTimeoutNs = 2000000000ull;  // 2 s per in-kernel wait
-// K/V bytes of the (b, h) slices one scheduling group spans: well under the
-// 129 MB L2, so that the CTAs running at one time re-read K/V tiles from L2.
-constexpr int64_t kL2GroupBytes = 48ll << 20;
+constexpr uint64_t kDefaultWaitTimeoutNs = ATTN_DEFAULT_WAIT_TIMEOUT_NS;
 constexpr int kMaxDevices = 64;
 // attn_fwd_staged: inputs per chunk, and the most chunks one call uses.
 constexpr int64_t kStagedChunkBytes = 48ll << 20;
@@ -66,10 +63,7 @@ bool staged_setup(StagedState& r) {
   return true;
 }
 
-bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
-  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return x < y + nb && y < x + na;
-}
+using ea::overlaps;
 
 // Validation common to every entry point; touches no CUDA API.
 attn_status_t validate(const void* q, const void* k, const void* v, const void* out,

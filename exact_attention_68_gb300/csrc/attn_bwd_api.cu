@@ -13,12 +13,8 @@
 
 namespace {
 
-constexpr uint64_t kDefaultWaitTimeoutNs = 2000000000ull;  // 2 s per in-kernel wait
-
-bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
-  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return x < y + nb && y < x + na;
-}
+constexpr uint64_t kDefaultWaitTimeoutNs = ATTN_DEFAULT_WAIT_TIMEOUT_NS;
+using ea::overlaps;
 
 // Checks of attn_bwd; touches no CUDA API.
 attn_status_t validate_bwd(const void* q, const void* k, const void* v, const void* out,

@@ -23,6 +23,12 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
                                  float scale, int causal, bool f16, uint64_t timeout_ns,
                                  int* status, cudaStream_t stream);
 
+// True if the byte ranges [a, a+na) and [b, b+nb) intersect.
+inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
 // The current device's status word pair (allocated on first use), after the
 // architecture check.
 attn_status_t current_status_words(int** status);

@@ -28,7 +28,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // same bound as attn_fwd
+constexpr uint64_t kWaitTimeoutNs = ATTN_DEFAULT_WAIT_TIMEOUT_NS;  // the bound attn_fwd uses
 // Scratch the forward kernel needs: its two status words.  The need does not
 // grow with B, H, S or D.
 constexpr size_t kScratchNeedBytes = 2 * sizeof(int);

@@ -55,6 +55,10 @@ EA_HOST_DEVICE void schedule_unit(const UnitSchedule& s, int x, int* bh, int* u)
   }
 }
 
+// K/V bytes of the (b, h) slices one phase-1 group spans: well under the
+// 129 MB L2, so that the CTAs running at one time re-read K/V tiles from L2.
+constexpr int64_t kL2GroupBytes = 48ll << 20;
+
 // Host choice of the schedule.  kv_group_bytes: K/V bytes one group may span;
 // sms: the device's SM count.  Phase 2 gets about sqrt(2·n_units·sms/BH)
 // levels: per SM roughly the cost of one of the heaviest units, which is the
