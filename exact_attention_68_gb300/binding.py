@@ -18,9 +18,9 @@ import torch
 from .build import LIB_PATH
 
 __all__ = ["AttnError", "load_library", "attn_fwd", "attn_fwd_bounded", "attn_fwd_staged",
-           "attn_fwd_noalloc", "attn_bwd", "attn_bwd_bounded", "device_status", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
-           "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_F16",
-           "EXPORTED_SYMBOLS"]
+           "attn_fwd_noalloc", "attn_bwd", "attn_bwd_bounded", "attention", "device_status",
+           "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
+           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_F16", "EXPORTED_SYMBOLS"]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
 ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 3, 4, 5
@@ -41,6 +41,7 @@ _SIGS = {
     "attn_device_status": (_i, [_p]),
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_abi_version": (_i, []),
+    "attn_last_cuda_error": (_i, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -52,7 +53,24 @@ class AttnError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
         msg = _status_string(code)
+        if code == ATTN_ERR_CUDA:
+            msg += f" ({_cuda_cause()})"
         super().__init__(f"{where}: {msg} (status {code})")
+
+
+def _cuda_cause() -> str:
+    """The library's record of the CUDA failure behind the last ATTN_ERR_CUDA."""
+    try:
+        c = int(load_library().attn_last_cuda_error())
+    except Exception:
+        return "cause unknown"
+    if c == -1:
+        return "TMA tensor map encode failed"
+    try:
+        from cuda.bindings import runtime as _rt
+        return f"{_rt.cudaError_t(c).name} ({c})"
+    except Exception:
+        return f"cudaError_t {c}"
 
 
 def load_library(path: str | None = None) -> ctypes.CDLL:
@@ -246,3 +264,29 @@ def device_status(device=None, stream=None) -> int:
     lib = load_library()
     with torch.cuda.device(dev):
         return int(lib.attn_device_status(_stream_handle(dev, stream)))
+
+
+class _AttentionFn(torch.autograd.Function):
+    """attn_fwd in forward, attn_bwd in backward (both through the C ABI)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal):
+        out, lse = attn_fwd(q, k, v, scale=scale, causal=causal)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.scale, ctx.causal = scale, causal
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        dq, dk, dv, _ = attn_bwd(q, k, v, out, lse, dout.contiguous(), scale=ctx.scale,
+                                 causal=ctx.causal)
+        return dq, dk, dv, None, None
+
+
+def attention(q, k, v, scale=None, causal=True):
+    """Differentiable fused attention: out = softmax(scale·q·kᵀ + mask)·v for
+    contiguous bf16/fp16 CUDA tensors [B, H, S, D]; gradients flow to q, k, v."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _AttentionFn.apply(q, k, v, float(scale), bool(causal))

@@ -98,7 +98,9 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
 // Per-device set-up on first use: architecture check and the status words.
 attn_status_t device_state(int* dev_out, DeviceState** st_out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  const cudaError_t e = ea::current_device_bound(&dev);
+  if (e != cudaSuccess) return ea::cuda_failure(static_cast<int>(e));
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& st = g_dev[dev];
   if (!st.ready) {
@@ -165,7 +167,7 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
       !encode_bhsd_16bit(&p.tm_k, k, BH, S, D, kBlockN, f16) ||
       !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, kBlockN, f16) ||
       !encode_bhsd_16bit(&p.tm_o, out, BH, S, D, 32, f16))
-    return ATTN_ERR_CUDA;
+    return cuda_failure(kErrTensorMap);
   p.lse = lse;
   p.status = status;
   p.B = static_cast<int>(B);
@@ -174,15 +176,16 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
   p.n_qt = static_cast<int>((S + kBlockM - 1) / kBlockM);
   p.n_units = (p.n_qt + kQTilesPerUnit - 1) / kQTilesPerUnit;
   int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_failure(static_cast<int>(e));
   p.sched = plan_schedule(BH, p.n_units, S, D, causal != 0, kL2GroupBytes, sms);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout_ns;
-  if (fwd_launch(p, static_cast<int>(D), causal != 0, f16, stream) != cudaSuccess) {
+  e = fwd_launch(p, static_cast<int>(D), causal != 0, f16, stream);
+  if (e != cudaSuccess) {
     (void)cudaGetLastError();
-    return ATTN_ERR_CUDA;
+    return cuda_failure(static_cast<int>(e));
   }
   return ATTN_OK;
 }
@@ -299,5 +302,7 @@ const char* attn_status_string(attn_status_t status) {
 }
 
 int attn_abi_version(void) { return 1; }
+
+int attn_last_cuda_error(void) { return ea::g_last_cuda_error; }
 
 }  // extern "C"

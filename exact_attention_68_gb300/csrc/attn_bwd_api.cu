@@ -71,7 +71,7 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
       !ea::encode_bhsd_16bit(&p.tm_dq, dq, BH, S, D, 32, f16) ||
       !ea::encode_bhsd_16bit(&p.tm_dk, dk, BH, S, D, 32, f16) ||
       !ea::encode_bhsd_16bit(&p.tm_dv, dv, BH, S, D, 32, f16))
-    return ATTN_ERR_CUDA;
+    return ea::cuda_failure(ea::kErrTensorMap);
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);
   p.v = static_cast<const uint16_t*>(v);
@@ -87,9 +87,10 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = wait_timeout_ns;
-  if (ea::bwd_launch(p, static_cast<int>(D), causal != 0, f16, stream) != cudaSuccess) {
+  const cudaError_t e = ea::bwd_launch(p, static_cast<int>(D), causal != 0, f16, stream);
+  if (e != cudaSuccess) {
     (void)cudaGetLastError();
-    return ATTN_ERR_CUDA;
+    return ea::cuda_failure(static_cast<int>(e));
   }
   return ATTN_OK;
 }

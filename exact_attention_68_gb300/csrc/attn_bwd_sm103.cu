@@ -820,12 +820,17 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvLayout<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>((long long)p.BH * p.n_t);
-  kdq<<<grid, kBwdThreads, DqLayout<D>::kAlloc, stream>>>(p);
-  e = cudaGetLastError();
+  // cudaLaunchKernelEx reports this launch's own status (no reliance on the
+  // thread's last-error state, which other code on the thread may have set)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((long long)p.BH * p.n_t), 1, 1);
+  cfg.blockDim = dim3(kBwdThreads, 1, 1);
+  cfg.stream = stream;
+  cfg.dynamicSmemBytes = DqLayout<D>::kAlloc;
+  e = cudaLaunchKernelEx(&cfg, kdq, p);
   if (e != cudaSuccess) return e;
-  kkv<<<grid, kBwdThreads, KvLayout<D>::kAlloc, stream>>>(p);
-  return cudaGetLastError();
+  cfg.dynamicSmemBytes = KvLayout<D>::kAlloc;
+  return cudaLaunchKernelEx(&cfg, kkv, p);
 }
 
 template <bool F16>

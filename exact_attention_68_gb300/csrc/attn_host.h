@@ -23,6 +23,25 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
                                  float scale, int causal, bool f16, uint64_t timeout_ns,
                                  int* status, cudaStream_t stream);
 
+// What the last ATTN_ERR_CUDA on this thread came from: a cudaError_t, or
+// kErrTensorMap when a TMA tensor map could not be encoded (0: none).
+constexpr int kErrTensorMap = -1;
+inline thread_local int g_last_cuda_error = 0;
+inline attn_status_t cuda_failure(int code) {
+  g_last_cuda_error = code;
+  return ATTN_ERR_CUDA;
+}
+
+// The calling thread's current device, with its primary context made current
+// on this thread: the TMA tensor maps are encoded by a driver call, which
+// needs a current context, and a thread that has only ever called
+// cudaGetDevice has none yet.
+inline cudaError_t current_device_bound(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e == cudaSuccess) e = cudaSetDevice(*dev);
+  return e;
+}
+
 // True if the byte ranges [a, a+na) and [b, b+nb) intersect.
 inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);

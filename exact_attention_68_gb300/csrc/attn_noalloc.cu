@@ -48,7 +48,11 @@ NoAllocDevice g_dev[kMaxDevices];
 // address of the scratch array.  Nothing is allocated.
 attn_status_t noalloc_setup(int** scratch) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  // binds the device's primary context to this thread (the tensor maps are
+  // encoded by a driver call); allocates nothing
+  const cudaError_t e = ea::current_device_bound(&dev);
+  if (e != cudaSuccess) return ea::cuda_failure(static_cast<int>(e));
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   NoAllocDevice& d = g_dev[dev];
   if (!d.ready) {

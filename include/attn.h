@@ -232,6 +232,13 @@ ATTN_API attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, 
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status_t status);
 
+/*
+ * The cause of the most recent ATTN_ERR_CUDA returned on the calling thread:
+ * the cudaError_t of the call that failed, or -1 when a TMA tensor map could
+ * not be encoded; 0 if no such error has been returned on this thread.
+ */
+ATTN_API int attn_last_cuda_error(void);
+
 /* ABI version of this library (incremented on any signature change). */
 ATTN_API int attn_abi_version(void);
 
