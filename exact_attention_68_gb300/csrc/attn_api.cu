@@ -73,7 +73,7 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
   if (B < 1 || H < 1 || S < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   // sizes: B·H and the grid fit int32, every byte count fits int64 (2^62)
   if (B > INT32_MAX || H > INT32_MAX || S > INT32_MAX) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = B * H;  // < 2^62, no overflow
@@ -81,6 +81,7 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
   const int64_t n_qt = (S + ea::kBlockM - 1) / ea::kBlockM;
   const int64_t n_units = (n_qt + ea::kQTilesPerUnit - 1) / ea::kQTilesPerUnit;
   if (BH * n_units > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+  if (D == 256 && BH * n_qt > INT32_MAX) return ATTN_ERR_INVALID_ARG;  // one CTA per Q tile
   if (BH > (int64_t(1) << 62) / (S * D * 2)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15u)
@@ -160,9 +161,32 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
                                  float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
                                  float scale, int causal, bool f16, uint64_t timeout_ns,
                                  int* status, cudaStream_t stream) {
+  const int64_t BH = B * H;
+  if (D == 256) {
+    Fwd256Params p;
+    std::memset(&p, 0, sizeof(p));
+    if (!encode_bhsd_16bit(&p.tm_k, k, BH, S, D, 64, f16) ||
+        !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, 64, f16) ||
+        !encode_bhsd_16bit(&p.tm_o, out, BH, S, D, 32, f16))
+      return cuda_failure(kErrTensorMap);
+    p.q = static_cast<const uint16_t*>(q);
+    p.lse = lse;
+    p.status = status;
+    p.BH = static_cast<int>(BH);
+    p.S = static_cast<int>(S);
+    p.n_qt = static_cast<int>((S + 127) / 128);
+    p.n_kt = static_cast<int>((S + 63) / 64);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.timeout_ns = timeout_ns;
+    const cudaError_t e = fwd256_launch(p, causal != 0, f16, stream);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return cuda_failure(static_cast<int>(e));
+    }
+    return ATTN_OK;
+  }
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
-  const int64_t BH = B * H;
   if (!encode_bhsd_16bit(&p.tm_q, q, BH, S, D, kBlockM, f16) ||
       !encode_bhsd_16bit(&p.tm_k, k, BH, S, D, kBlockN, f16) ||
       !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, kBlockN, f16) ||

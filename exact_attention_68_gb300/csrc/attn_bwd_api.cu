@@ -24,6 +24,7 @@ attn_status_t validate_bwd(const void* q, const void* k, const void* v, const vo
   // shapes, scale, mask flag, q/k/v/out/lse pointers and alignment
   attn_status_t s = ea::validate_args(q, k, v, out, lse, B, H, S, D, scale, causal);
   if (s != ATTN_OK) return s;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;  // the backward: D = 64, 128
   if (!dout || !dq || !dk || !dv || !delta) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u)

@@ -39,6 +39,23 @@ struct FwdParams {
   uint64_t timeout_ns;
 };
 
+// Head dimension 256: one 128-row Q tile per CTA, 64-row K/V tiles, Q in TMEM.
+struct Fwd256Params {
+  CUtensorMap tm_k;    // k as (256, S, B·H), box 64 x 64 rows, 128-byte swizzle
+  CUtensorMap tm_v;    // v, same box
+  CUtensorMap tm_o;    // out, box 64 x 32 rows
+  const uint16_t* q;   // 16-bit [B·H, S, 256]: rows read into TMEM
+  float* lse;          // [B·H, S]
+  int* status;
+  int BH, S;
+  int n_qt;            // ceil(S / 128)
+  int n_kt;            // ceil(S / 64)
+  float scale_log2;
+  uint64_t timeout_ns;
+};
+
+cudaError_t fwd256_launch(const Fwd256Params& p, bool causal, bool f16, cudaStream_t stream);
+
 // Dynamic shared memory one CTA of the D-specialised kernel uses.
 size_t fwd_smem_bytes(int D);
 

@@ -1,0 +1,390 @@
+// attn_fwd_d256_sm103.cu — the fused attention forward for head dimension 256
+// on GB300 (sm_103a).
+//
+// Same computation as the D = 64 / 128 kernel: out = softmax(scale·q·kᵀ +
+// causal mask)·v per (batch, head) with the row logsumexp, following the five
+// steps of "Profiling in PyTorch (Part 3): Attention is all you profile",
+// section "Naive attention", walked tile by tile with a running softmax so the
+// [S, S] scores never leave the chip (same page, "Why flash attention exists";
+// FlashAttention-2 blog, "FlashAttention-2 Optimizations" §1-§3).
+//
+// At D = 256 two Q tiles' O accumulators would fill TMEM on their own, so the
+// layout differs: one 128-row Q tile per CTA, K/V tiles of 64 rows, and two
+// 64-column S buffers so that the next S is computed while the softmax of the
+// current one runs.  Q is the A operand of every S product of the CTA: it is
+// put into TMEM once, so S = Q·Kᵀ is a TS product and shared memory only feeds
+// K and V.  TMEM columns: S_b [64b, 64b+64) (P_b, 16-bit, over its first 32),
+// Q [128, 256) (two 16-bit values per column), O [256, 512).
+//
+// Roles (192 threads): warps 0-3 softmax / correction / epilogue, one thread
+// per query row (TMEM lane); warp 4 issues tcgen05.mma and owns TMEM; warp 5
+// feeds the K and V rings with TMA.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn_fwd.h"
+#include "ptx.cuh"
+#include "umma.cuh"
+
+namespace ea {
+namespace {
+
+constexpr int kD = 256;
+constexpr int kKvRows = 64;                      // rows of one K/V tile
+constexpr int kQRows = 128;                      // rows of the Q tile
+constexpr int kThreads256 = 192;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;        // log2 units, as in the D <= 128 kernel
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+constexpr int kChunkBytes = kKvRows * 128;       // one 64-column block of a K/V tile (8 KB)
+constexpr int kTile = kKvRows * kD * 2;          // one K/V tile (32 KB)
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
+constexpr int kKOff = 0;
+constexpr int kVOff = kKOff + kKStages * kTile;
+constexpr int kBarOff = kVOff + kVStages * kTile;
+constexpr int kKFull = 0, kKEmpty = kKFull + kKStages, kVFull = kKEmpty + kKStages,
+              kVEmpty = kVFull + kVStages, kSFull = kVEmpty + kVStages,  // [2]
+              kPFull = kSFull + 2,                                         // [2], 128 arrivals
+              kQTmem = kPFull + 2,                                         // 128 arrivals
+              kPvDone = kQTmem + 1, kOFull = kPvDone + 1, kDrain = kOFull + 1,
+              kNumBars = kDrain + 1;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kAlloc = kMiscOff + 16 + 1024;
+static_assert(kAlloc <= 232448, "shared memory budget exceeded");
+// the epilogue stages O (128 rows x 256 bf16 = 64 KB) in the K ring
+static_assert(kKStages * kTile >= kQRows * kD * 2, "O staging must fit the K ring");
+constexpr uint32_t kQCol = 128, kOCol = 256, kTmemCols = 512;
+
+enum : int { kSiteProdK = 0x3100, kSiteProdV = 0x3200, kSiteMmaQ = 0x3300, kSiteMmaK = 0x3400,
+             kSiteMmaV = 0x3500, kSiteMmaP = 0x3600, kSiteSoftS = 0x3700, kSiteSoftPv = 0x3800,
+             kSiteSoftO = 0x3900 };
+
+template <bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(kThreads256, 1) attn_fwd_d256_kernel(const __grid_constant__ Fwd256Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  auto bar = [sb](int idx) -> uint32_t { return sb + kBarOff + 8u * idx; };
+  const uint32_t tmem_slot = sb + kMiscOff;
+  const uint32_t abort_addr = sb + kMiscOff + 4;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Q tile i of slice bh, the tiles with the most keys first
+  const int level = blockIdx.x / p.BH;
+  const int bh = blockIdx.x - level * p.BH;
+  const int i = p.n_qt - 1 - level;
+  int nkv = CAUSAL ? 2 * i + 2 : p.n_kt;  // K/V tiles this Q tile meets
+  if (nkv > p.n_kt) nkv = p.n_kt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKEmpty + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(bar(kVFull + s), 1);
+      mbar_init(bar(kVEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kSFull + b), 1);
+      mbar_init(bar(kPFull + b), 128);
+    }
+    mbar_init(bar(kQTmem), 128);
+    mbar_init(bar(kPvDone), 1);
+    mbar_init(bar(kOFull), 1);
+    mbar_init(bar(kDrain), 1);
+    st_volatile_shared(abort_addr, 0);
+    fence_barrier_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = static_cast<uint32_t>(ld_volatile_shared(tmem_slot));
+  const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
+
+  if (warp < 4) {
+    // ======================= softmax / correction / epilogue =======================
+    const int row = warp * 32 + lane;
+    const int grow = i * kQRows + row;
+    const bool valid = grow < p.S;
+    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tO = tmem_base + lane_bits + kOCol;
+    {
+      // this row of Q into TMEM, 64 columns (128 values) per store
+      const int64_t qrow = valid ? (int64_t)bh * p.S + grow : 0;  // rows past S load nothing
+      const uint4* q4 = reinterpret_cast<const uint4*>(p.q + qrow * kD);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = valid ? __ldg(q4 + 8 * c + u) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * u] = x.x, w[4 * u + 1] = x.y, w[4 * u + 2] = x.z, w[4 * u + 3] = x.w;
+        }
+        tmem_st_32x32b_x32(tmem_base + lane_bits + kQCol + 32 * c, w);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(kQTmem));
+    }
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // reference max (log2 units) of the exponentials in O and l
+    float l = 0.f;        // running sum of p: gives the logsumexp
+    float lq = 0.f;       // l plus each tile's rounding error of its largest p (normalises O)
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int b = j & 1;
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(kSFull + b), (j >> 1) & 1, ctl,
+                                                kSiteSoftS | (j & 0xff)));
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t tS = tmem_base + lane_bits + 64 * b;
+      uint32_t s[2][32];
+      tmem_ld_32x32b_x32(tS, s[0]);
+      tmem_ld_32x32b_x32(tS + 32, s[1]);
+      tmem_ld_wait();
+      reg_fence(s[0]);
+      reg_fence(s[1]);
+      // allowed key columns of this tile: 0 .. lim (causal: key <= query; key < S)
+      int lim = p.S - 1 - j * kKvRows;
+      if (CAUSAL) lim = min(lim, grow - j * kKvRows);
+      if (!valid) lim = -1;
+      if (lim < 63) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c > lim) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
+#pragma unroll
+      for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(s[c >> 5][c & 31]));
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      const float m_tile = mx * sl2;
+      float alpha = 1.f;
+      bool moved = false;
+      if (m == -INFINITY) {
+        m = m_tile;  // first tile with an allowed key sets the reference
+      } else if (m_tile > m + kRescaleThreshold) {
+        alpha = ex2_approx(m - m_tile);
+        m = m_tile;
+        moved = true;
+      }
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int e2 = 0; e2 < 32; ++e2) {
+        const int h = e2 >> 4, e = (2 * e2) & 31;
+        const float p0 = ex2_approx(fmaf(__uint_as_float(s[h][e]), sl2, neg_m));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(s[h][e + 1]), sl2, neg_m));
+        rs0 += p0;
+        rs1 += p1;
+        pk[e2] = pack_x2<F16>(p0, p1);
+      }
+      tmem_st_32x32b_x32(tS, pk);
+      const float rs = rs0 + rs1;
+      const float pmax = ex2_approx(fmaf(mx, sl2, neg_m));
+      l = l * alpha + rs;
+      lq = lq * alpha + (rs + (round_to_x<F16>(pmax) - pmax));
+      // correction: O of a row whose reference moved is rescaled before PV_j
+      // accumulates into it; PV_{j-1} must have completed first
+      if (__any_sync(0xffffffffu, moved)) {
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, wait_bounded(bar(kPvDone), (j - 1) & 1, ctl,
+                                                    kSiteSoftPv | (j & 0xff)));
+          if (!ok) break;
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tO + 32 * c, o);
+            tmem_ld_wait();
+            reg_fence(o);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+            tmem_st_32x32b_x32(tO + 32 * c, o);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(kPFull + b));
+    }
+
+    // ---- epilogue: O / lq → 16-bit → swizzled staging (K ring) → TMA store; lse
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(kOFull), 0, ctl, kSiteSoftO));
+    if (ok) {
+      tc_fence_after_sync();
+      const float inv_l = lq > 0.f ? 1.f / lq : 0.f;
+      // 4 column blocks of 64 (128 bytes per row), 128 rows each (16 KB)
+#pragma unroll 1
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tO + 32 * c, o);
+        tmem_ld_wait();
+        reg_fence(o);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int unit = (c & 1) * 4 + q4;  // 16-byte unit within the 128-byte row
+          const uint32_t addr = sb + kKOff + (c >> 1) * (kQRows * 128) + row * 128 +
+                                ((unit ^ (row & 7)) << 4);
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_x2<F16>(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
+                                __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
+          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < kD / 64; ++c)
+          tma_store_3d(&p.tm_o, sb + kKOff + c * (kQRows * 128) + warp * 32 * 128, c * 64,
+                       i * kQRows + warp * 32, bh);
+        tma_store_commit();
+      }
+      if (valid) p.lse[(int64_t)bh * p.S + grow] = (m + __log2f(l)) * kLn2;
+      if (lane == 0) tma_store_wait_all();
+    }
+    tc_fence_before_sync();
+  } else if (warp == 5) {
+    // ======================= TMA producer: K and V rings =======================
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_o);
+      const uint64_t pol = l2_policy_evict_last();
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        const int ks = j % kKStages;
+        ok = wait_bounded(bar(kKEmpty + ks), ((j / kKStages) & 1) ^ 1, ctl, kSiteProdK | (j & 0xff));
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(kKFull + ks), kTile);
+#pragma unroll
+        for (int c = 0; c < kD / 64; ++c)
+          tma_load_3d(sb + kKOff + ks * kTile + c * kChunkBytes, &p.tm_k, bar(kKFull + ks), c * 64,
+                      j * kKvRows, bh, pol);
+        k_issued = j + 1;
+        const int vs = j % kVStages;
+        ok = wait_bounded(bar(kVEmpty + vs), ((j / kVStages) & 1) ^ 1, ctl, kSiteProdV | (j & 0xff));
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(kVFull + vs), kTile);
+#pragma unroll
+        for (int c = 0; c < kD / 64; ++c)
+          tma_load_3d(sb + kVOff + vs * kTile + c * kChunkBytes, &p.tm_v, bar(kVFull + vs), c * 64,
+                      j * kKvRows, bh, pol);
+        v_issued = j + 1;
+      }
+      if (ok) {
+        for (int j = max(nkv - kKStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(bar(kKEmpty + j % kKStages), (j / kKStages) & 1, ctl, kSiteProdK | 0xff);
+        for (int j = max(nkv - kVStages, 0); j < nkv && ok; ++j)
+          ok = wait_bounded(bar(kVEmpty + j % kVStages), (j / kVStages) & 1, ctl, kSiteProdV | 0xff);
+      }
+      if (!ok) {
+        for (int j = max(k_issued - kKStages, 0); j < k_issued; ++j)
+          wait_drain(bar(kKFull + j % kKStages), (j / kKStages) & 1, kDrainLimitNs);
+        for (int j = max(v_issued - kVStages, 0); j < v_issued; ++j)
+          wait_drain(bar(kVFull + j % kVStages), (j / kVStages) & 1, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ======================= tcgen05 issuer (warp 4) =======================
+    const bool leader = elect_one();
+    constexpr uint32_t kIdescS = instr_desc_16bit(kQRows, kKvRows, false, false, F16);
+    constexpr uint32_t kIdescO = instr_desc_16bit(kQRows, kD, false, true, F16);
+    constexpr uint32_t kTileUnits = kTile >> 4;
+    const uint64_t dk = smem_desc_sw128(sb + kKOff, 16, 1024);
+    const uint64_t dv = smem_desc_sw128(sb + kVOff, kChunkBytes, 1024);
+    auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
+      return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
+    };
+    // S(j) into buffer j & 1: Q (TMEM, 8 columns per K step) · K_jᵀ (K-major)
+    auto issue_s = [&](int j) {
+      const uint64_t db = dk + (j % kKStages) * kTileUnits;
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ts(tmem_base + 64 * (j & 1), tmem_base + kQCol + kk * 8, db + off, kIdescS,
+               kk > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(kSFull + (j & 1)));
+      mma_commit(bar(kKEmpty + j % kKStages));
+    };
+    bool ok = wait_warp(bar(kQTmem), 0, kSiteMmaQ);
+    for (int j0 = 0; j0 < 2 && j0 < nkv && ok; ++j0) {
+      ok = wait_warp(bar(kKFull + j0 % kKStages), (j0 / kKStages) & 1, kSiteMmaK | j0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) issue_s(j0);
+      __syncwarp();
+    }
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int b = j & 1;
+      ok = wait_warp(bar(kPFull + b), (j >> 1) & 1, kSiteMmaP | (j & 0xff));
+      if (ok) ok = wait_warp(bar(kVFull + j % kVStages), (j / kVStages) & 1, kSiteMmaV | (j & 0xff));
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) {
+        const uint64_t db = dv + (j % kVStages) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < kKvRows / 16; ++kk)  // O += P_b · V_j, 16 keys per step
+          mma_ts(tmem_base + kOCol, tmem_base + 64 * b + kk * 8, db + kk * (2048 >> 4), kIdescO,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(kPvDone));
+        mma_commit(bar(kVEmpty + j % kVStages));
+      }
+      __syncwarp();
+      if (j + 2 < nkv) {
+        ok = wait_warp(bar(kKFull + (j + 2) % kKStages), ((j + 2) / kKStages) & 1,
+                       kSiteMmaK | ((j + 2) & 0xff));
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (leader) issue_s(j + 2);  // overwrites P_b: PV_j was issued first
+        __syncwarp();
+      }
+    }
+    if (leader) {
+      if (ok) mma_commit(bar(kOFull));
+      mma_commit(bar(kDrain));
+      wait_drain(bar(kDrain), 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <bool CAUSAL, bool F16>
+cudaError_t launch_d256(const Fwd256Params& p, cudaStream_t stream) {
+  auto kern = attn_fwd_d256_kernel<CAUSAL, F16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((long long)p.BH * p.n_qt), 1, 1);
+  cfg.blockDim = dim3(kThreads256, 1, 1);
+  cfg.dynamicSmemBytes = kAlloc;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+cudaError_t fwd256_launch(const Fwd256Params& p, bool causal, bool f16, cudaStream_t stream) {
+  if (f16) return causal ? launch_d256<true, true>(p, stream) : launch_d256<false, true>(p, stream);
+  return causal ? launch_d256<true, false>(p, stream) : launch_d256<false, false>(p, stream);
+}
+
+}  // namespace ea

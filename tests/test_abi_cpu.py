@@ -63,7 +63,8 @@ def _call(lib, q=A, k=A + T, v=A + 2 * T, out=A + 3 * T, lse=A + 4 * T,
     (dict(S=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(D=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(D=96), binding.ATTN_ERR_UNSUPPORTED),
-    (dict(D=256), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(D=512), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(D=32), binding.ATTN_ERR_UNSUPPORTED),
     (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
     (dict(scale=-0.5), binding.ATTN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), binding.ATTN_ERR_INVALID_ARG),
@@ -125,6 +126,7 @@ def _bwd(lib, q=A, k=A + T, v=A + 2 * T, out=A + 3 * T, lse=A + 4 * T, dout=A + 
     (dict(delta=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(S=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(D=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), binding.ATTN_ERR_UNSUPPORTED),   # the forward has D=256, the backward not
     (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
     (dict(causal=3), binding.ATTN_ERR_INVALID_ARG),
     (dict(dout=A + 5 * T + 8), binding.ATTN_ERR_MISALIGNED),

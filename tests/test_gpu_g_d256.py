@@ -1,0 +1,62 @@
+"""GPU parity of the head-dimension-256 forward (its own kernel: one Q tile
+per CTA, 64-row K/V tiles, Q in TMEM) against the fp64 oracle, with the same
+bar as the D = 64 / 128 forward."""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_68_gb300 import binding
+from exact_attention_68_gb300.workloads import default_scale, make_qkv
+from gpu_helpers import compare, run_gpu, to_f64
+from oracle import attention_fwd, attention_rows
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(1, 1, 1, 256), (1, 1, 7, 256), (1, 2, 63, 256), (1, 2, 64, 256), (2, 1, 65, 256),
+          (1, 2, 128, 256), (2, 2, 129, 256), (1, 2, 200, 256), (1, 1, 513, 256), (1, 2, 1000, 256)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+def test_d256_full_oracle(cuda_device, shape, causal, dtype):
+    q, k, v = make_qkv(shape, seed=91, dtype=dtype)
+    scale = default_scale(256)
+    out, lse = run_gpu(q, k, v, scale, causal)
+    assert out.dtype == dtype
+    ro, rl = attention_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), scale, causal)
+    compare(to_f64(out), to_f64(lse), ro, rl, f"D=256 {shape} causal={causal} {dtype}")
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_d256_peaked_softmax_moves_the_reference_max(cuda_device, causal):
+    """q, k ~ N(0, 3^2): logits spread far enough that rows' running max moves
+    by more than the threshold, so the O correction path runs."""
+    shape = (2, 2, 700, 256)
+    q, k, v = make_qkv(shape, seed=92, qk_std=3.0)
+    scale = default_scale(256)
+    out, lse = run_gpu(q, k, v, scale, causal)
+    ro, rl = attention_fwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), scale, causal)
+    compare(to_f64(out), to_f64(lse), ro, rl, f"D=256 peaked causal={causal}")
+
+
+def test_d256_long_sequence_sampled_rows(cuda_device):
+    B, H, S = 1, 8, 8192
+    q, k, v = make_qkv((B, H, S, 256), seed=93)
+    scale = default_scale(256)
+    out, lse = run_gpu(q, k, v, scale, True)
+    rng = np.random.default_rng(94)
+    idx = np.stack([np.zeros(400, np.int64), rng.integers(0, H, 400), rng.integers(0, S, 400)], 1)
+    idx = np.concatenate([idx, [[0, h, r] for h in range(H) for r in (0, 127, 128, S - 1)]]).astype(np.int64)
+    ro, rl = attention_rows(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, True, idx)
+    og = to_f64(out)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    lg = to_f64(lse)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    compare(og, lg, ro, rl, "D=256 S=8192")
+
+
+def test_d256_backward_is_refused(cuda_device):
+    q, k, v = (x.to("cuda:0") for x in make_qkv((1, 1, 128, 256), seed=95))
+    out, lse = binding.attn_fwd(q, k, v, causal=True)
+    with pytest.raises(binding.AttnError) as e:
+        binding.attn_bwd(q, k, v, out, lse, torch.ones_like(q), causal=True)
+    assert e.value.code == binding.ATTN_ERR_UNSUPPORTED
