@@ -178,7 +178,7 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
     p.n_kt = static_cast<int>((S + 63) / 64);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.timeout_ns = timeout_ns;
-    const cudaError_t e = fwd256_launch(p, causal != 0, f16, stream);
+    const cudaError_t e = fwd1q_launch(p, 256, causal != 0, f16, stream);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       return cuda_failure(static_cast<int>(e));
@@ -317,7 +317,8 @@ const char* attn_status_string(attn_status_t status) {
   switch (status) {
     case ATTN_OK: return "ok";
     case ATTN_ERR_INVALID_ARG: return "invalid argument";
-    case ATTN_ERR_UNSUPPORTED: return "unsupported (head_dim must be 64 or 128; device must be sm_103)";
+    case ATTN_ERR_UNSUPPORTED:
+      return "unsupported (head_dim must be 64, 128 or, forward only, 256; device must be sm_103)";
     case ATTN_ERR_MISALIGNED: return "misaligned pointer (q/k/v/out need 16 bytes, lse 4 bytes)";
     case ATTN_ERR_CUDA: return "CUDA call failed";
     case ATTN_ERR_TIMEOUT: return "an in-kernel wait ran out of time";

@@ -54,7 +54,8 @@ struct Fwd256Params {
   uint64_t timeout_ns;
 };
 
-cudaError_t fwd256_launch(const Fwd256Params& p, bool causal, bool f16, cudaStream_t stream);
+// One Q tile per CTA, 64-row K/V tiles, Q in TMEM (used for D = 256).
+cudaError_t fwd1q_launch(const Fwd256Params& p, int D, bool causal, bool f16, cudaStream_t stream);
 
 // Dynamic shared memory one CTA of the D-specialised kernel uses.
 size_t fwd_smem_bytes(int D);

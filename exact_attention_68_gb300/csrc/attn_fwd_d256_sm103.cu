@@ -30,39 +30,52 @@
 namespace ea {
 namespace {
 
-constexpr int kD = 256;
 constexpr int kKvRows = 64;                      // rows of one K/V tile
 constexpr int kQRows = 128;                      // rows of the Q tile
-constexpr int kThreads256 = 192;
+constexpr int kThreads1Q = 192;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;        // log2 units, as in the D <= 128 kernel
+constexpr float kRescaleThreshold = 8.0f;        // log2 units, as in the two-tile kernel
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 constexpr int kChunkBytes = kKvRows * 128;       // one 64-column block of a K/V tile (8 KB)
-constexpr int kTile = kKvRows * kD * 2;          // one K/V tile (32 KB)
-constexpr int kKStages = 3;
-constexpr int kVStages = 3;
-constexpr int kKOff = 0;
-constexpr int kVOff = kKOff + kKStages * kTile;
-constexpr int kBarOff = kVOff + kVStages * kTile;
-constexpr int kKFull = 0, kKEmpty = kKFull + kKStages, kVFull = kKEmpty + kKStages,
-              kVEmpty = kVFull + kVStages, kSFull = kVEmpty + kVStages,  // [2]
-              kPFull = kSFull + 2,                                         // [2], 128 arrivals
-              kQTmem = kPFull + 2,                                         // 128 arrivals
-              kPvDone = kQTmem + 1, kOFull = kPvDone + 1, kDrain = kOFull + 1,
-              kNumBars = kDrain + 1;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kAlloc = kMiscOff + 16 + 1024;
-static_assert(kAlloc <= 232448, "shared memory budget exceeded");
-// the epilogue stages O (128 rows x 256 bf16 = 64 KB) in the K ring
-static_assert(kKStages * kTile >= kQRows * kD * 2, "O staging must fit the K ring");
-constexpr uint32_t kQCol = 128, kOCol = 256, kTmemCols = 512;
+
+template <int D>
+struct Layout1Q {
+  static constexpr int kTile = kKvRows * D * 2;  // one K/V tile
+  static constexpr int kKStages = (D == 256) ? 3 : 5;
+  static constexpr int kVStages = (D == 256) ? 3 : 5;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kKStages * kTile;
+  static constexpr int kBarOff = kVOff + kVStages * kTile;
+  static constexpr int kKFull = 0, kKEmpty = kKFull + kKStages, kVFull = kKEmpty + kKStages,
+                       kVEmpty = kVFull + kVStages, kSFull = kVEmpty + kVStages,  // [2]
+                       kPFull = kSFull + 2,                                         // [2], 128
+                       kQTmem = kPFull + 2,                                         // 128 arrivals
+                       kPvDone = kQTmem + 1, kOFull = kPvDone + 1, kDrain = kOFull + 1,
+                       kNumBars = kDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kAlloc = kMiscOff + 16 + 1024;
+  static_assert(kAlloc <= 232448, "shared memory budget exceeded");
+  // the epilogue stages O (128 rows x D 16-bit values) in the K ring
+  static_assert(kKStages * kTile >= kQRows * D * 2, "O staging must fit the K ring");
+  static constexpr uint32_t kQCol = 128, kOCol = 256, kTmemCols = 512;
+  static_assert(kQCol + D / 2 <= kOCol && kOCol + D <= kTmemCols, "TMEM budget exceeded");
+};
 
 enum : int { kSiteProdK = 0x3100, kSiteProdV = 0x3200, kSiteMmaQ = 0x3300, kSiteMmaK = 0x3400,
              kSiteMmaV = 0x3500, kSiteMmaP = 0x3600, kSiteSoftS = 0x3700, kSiteSoftPv = 0x3800,
              kSiteSoftO = 0x3900 };
 
-template <bool CAUSAL, bool F16>
-__global__ void __launch_bounds__(kThreads256, 1) attn_fwd_d256_kernel(const __grid_constant__ Fwd256Params p) {
+template <int D, bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid_constant__ Fwd256Params p) {
+  using L = Layout1Q<D>;
+  constexpr int kD = D;
+  constexpr int kTile = L::kTile;
+  constexpr int kKStages = L::kKStages, kVStages = L::kVStages;
+  constexpr int kKOff = L::kKOff, kVOff = L::kVOff, kBarOff = L::kBarOff, kMiscOff = L::kMiscOff;
+  constexpr int kKFull = L::kKFull, kKEmpty = L::kKEmpty, kVFull = L::kVFull, kVEmpty = L::kVEmpty;
+  constexpr int kSFull = L::kSFull, kPFull = L::kPFull, kQTmem = L::kQTmem, kPvDone = L::kPvDone;
+  constexpr int kOFull = L::kOFull, kDrain = L::kDrain;
+  constexpr uint32_t kQCol = L::kQCol, kOCol = L::kOCol, kTmemCols = L::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
   auto bar = [sb](int idx) -> uint32_t { return sb + kBarOff + 8u * idx; };
@@ -116,11 +129,11 @@ __global__ void __launch_bounds__(kThreads256, 1) attn_fwd_d256_kernel(const __g
     const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tO = tmem_base + lane_bits + kOCol;
     {
-      // this row of Q into TMEM, 64 columns (128 values) per store
+      // this row of Q into TMEM, 32 columns (64 values) per store
       const int64_t qrow = valid ? (int64_t)bh * p.S + grow : 0;  // rows past S load nothing
       const uint4* q4 = reinterpret_cast<const uint4*>(p.q + qrow * kD);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kD / 64; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -367,14 +380,15 @@ __global__ void __launch_bounds__(kThreads256, 1) attn_fwd_d256_kernel(const __g
   }
 }
 
-template <bool CAUSAL, bool F16>
-cudaError_t launch_d256(const Fwd256Params& p, cudaStream_t stream) {
-  auto kern = attn_fwd_d256_kernel<CAUSAL, F16>;
+template <int D, bool CAUSAL, bool F16>
+cudaError_t launch_1q(const Fwd256Params& p, cudaStream_t stream) {
+  auto kern = attn_fwd_1q_kernel<D, CAUSAL, F16>;
+  constexpr int kAlloc = Layout1Q<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((long long)p.BH * p.n_qt), 1, 1);
-  cfg.blockDim = dim3(kThreads256, 1, 1);
+  cfg.blockDim = dim3(kThreads1Q, 1, 1);
   cfg.dynamicSmemBytes = kAlloc;
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, kern, p);
@@ -382,9 +396,12 @@ cudaError_t launch_d256(const Fwd256Params& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t fwd256_launch(const Fwd256Params& p, bool causal, bool f16, cudaStream_t stream) {
-  if (f16) return causal ? launch_d256<true, true>(p, stream) : launch_d256<false, true>(p, stream);
-  return causal ? launch_d256<true, false>(p, stream) : launch_d256<false, false>(p, stream);
+cudaError_t fwd1q_launch(const Fwd256Params& p, int D, bool causal, bool f16, cudaStream_t stream) {
+  // The layout also works at D = 128 (parity-checked), but there one Q tile's
+  // softmax is not covered by its products: the two-tile kernel is faster.
+  if (D != 256) return cudaErrorInvalidValue;
+  if (f16) return causal ? launch_1q<256, true, true>(p, stream) : launch_1q<256, false, true>(p, stream);
+  return causal ? launch_1q<256, true, false>(p, stream) : launch_1q<256, false, false>(p, stream);
 }
 
 }  // namespace ea
