@@ -35,17 +35,20 @@ from exact_attention_68_gb300.workloads import (WORKLOADS, Workload, algorithmic
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "causal bf16 attention fwd TFLOP/s on 1 GB300 and % of dense-BF16 peak"
 WORKLOAD = "c5"
-# The forward kernel's device code and the grid schedule it runs (the host
-# plan, including the L2 group size, lives in schedule.h).
-KERNEL_SOURCES = ["exact_attention_68_gb300/csrc/attn_fwd_sm103.cu",
+# The forward kernels' device code (the one-Q-tile kernel runs the causal
+# D=128 workload, the two-tile kernel the non-causal and D=64 side workloads)
+# and the two-tile kernel's grid schedule (schedule.h).
+KERNEL_SOURCES = ["exact_attention_68_gb300/csrc/attn_fwd_1q_sm103.cu",
+                  "exact_attention_68_gb300/csrc/attn_fwd_sm103.cu",
                   "exact_attention_68_gb300/csrc/ptx.cuh", "exact_attention_68_gb300/csrc/umma.cuh",
                   "exact_attention_68_gb300/csrc/attn_fwd.h", "exact_attention_68_gb300/csrc/schedule.h"]
 # DRAM bytes (read + write) per launch of the forward kernel on the default
 # workload, from ncu captures, keyed by the hash of the kernel sources they
 # were taken on (a changed kernel reports null until captured again).
 NCU_TRAFFIC_BYTES = {
-    # B=1 H=32 S=16384 D=128 causal: 829,026,816 read + 113,126,656 written
-    "d293ec5609ef90f2": 942153472,
+    # B=1 H=32 S=16384 D=128 causal (attn_fwd_1q_kernel<128,128,true>):
+    # 603,648,512 read + 117,861,888 written
+    "08bd8a0376c35a6a": 721510400,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -413,7 +416,7 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst, cuBLAS 8192^3)",
-                     "kernel": "attn_fwd_kernel<128,true>",
+                     "kernel": "attn_fwd_1q_kernel<128,128,true>",
                      "algorithmic_flops_per_launch": flops,
                      "algorithmic_bytes_per_launch": algorithmic_bytes(w.B, w.H, w.S, w.D)},
         "e2e": {"value": flops * e2e_steps / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",

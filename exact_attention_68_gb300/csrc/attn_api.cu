@@ -162,11 +162,14 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
                                  float scale, int causal, bool f16, uint64_t timeout_ns,
                                  int* status, cudaStream_t stream) {
   const int64_t BH = B * H;
-  if (D == 256) {
-    Fwd256Params p;
+  // One Q tile per CTA for D = 256, and for causal D = 128 (measured faster
+  // there); the two-tile kernel otherwise.
+  if (D == 256 || (D == 128 && causal != 0)) {
+    const int bn = D == 256 ? 64 : 128;  // rows of one K/V tile
+    Fwd1QParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!encode_bhsd_16bit(&p.tm_k, k, BH, S, D, 64, f16) ||
-        !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, 64, f16) ||
+    if (!encode_bhsd_16bit(&p.tm_k, k, BH, S, D, bn, f16) ||
+        !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, bn, f16) ||
         !encode_bhsd_16bit(&p.tm_o, out, BH, S, D, 32, f16))
       return cuda_failure(kErrTensorMap);
     p.q = static_cast<const uint16_t*>(q);
@@ -175,10 +178,15 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
     p.BH = static_cast<int>(BH);
     p.S = static_cast<int>(S);
     p.n_qt = static_cast<int>((S + 127) / 128);
-    p.n_kt = static_cast<int>((S + 63) / 64);
+    p.n_kt = static_cast<int>((S + bn - 1) / bn);
+    int dev1 = 0, sms1 = 0;
+    cudaError_t e1 = cudaGetDevice(&dev1);
+    if (e1 == cudaSuccess) e1 = cudaDeviceGetAttribute(&sms1, cudaDevAttrMultiProcessorCount, dev1);
+    if (e1 != cudaSuccess) return cuda_failure(static_cast<int>(e1));
+    p.sched = plan_schedule(BH, p.n_qt, S, D, causal != 0, kL2GroupBytes, sms1);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.timeout_ns = timeout_ns;
-    const cudaError_t e = fwd1q_launch(p, 256, causal != 0, f16, stream);
+    const cudaError_t e = fwd1q_launch(p, static_cast<int>(D), causal != 0, f16, stream);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       return cuda_failure(static_cast<int>(e));

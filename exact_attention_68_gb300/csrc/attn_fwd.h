@@ -39,23 +39,26 @@ struct FwdParams {
   uint64_t timeout_ns;
 };
 
-// Head dimension 256: one 128-row Q tile per CTA, 64-row K/V tiles, Q in TMEM.
-struct Fwd256Params {
-  CUtensorMap tm_k;    // k as (256, S, B·H), box 64 x 64 rows, 128-byte swizzle
+// The one-Q-tile kernel: one 128-row Q tile per CTA, Q in TMEM, BN-row K/V
+// tiles (BN = 64 at D = 256, 128 at D = 128).
+struct Fwd1QParams {
+  CUtensorMap tm_k;    // k as (D, S, B·H), box 64 x BN rows, 128-byte swizzle
   CUtensorMap tm_v;    // v, same box
   CUtensorMap tm_o;    // out, box 64 x 32 rows
-  const uint16_t* q;   // 16-bit [B·H, S, 256]: rows read into TMEM
+  const uint16_t* q;   // 16-bit [B·H, S, D]: rows read into TMEM
   float* lse;          // [B·H, S]
   int* status;
   int BH, S;
   int n_qt;            // ceil(S / 128)
-  int n_kt;            // ceil(S / 64)
+  int n_kt;            // ceil(S / BN)
+  UnitSchedule sched;  // CTA index -> (b·H + h, Q tile): a unit is one Q tile here
   float scale_log2;
   uint64_t timeout_ns;
 };
 
-// One Q tile per CTA, 64-row K/V tiles, Q in TMEM (used for D = 256).
-cudaError_t fwd1q_launch(const Fwd256Params& p, int D, bool causal, bool f16, cudaStream_t stream);
+// One Q tile per CTA, Q in TMEM: D = 256 (64-row K/V tiles) and D = 128
+// (128-row K/V tiles).
+cudaError_t fwd1q_launch(const Fwd1QParams& p, int D, bool causal, bool f16, cudaStream_t stream);
 
 // Dynamic shared memory one CTA of the D-specialised kernel uses.
 size_t fwd_smem_bytes(int D);

@@ -1,5 +1,5 @@
-// attn_fwd_d256_sm103.cu — the fused attention forward for head dimension 256
-// on GB300 (sm_103a).
+// attn_fwd_1q_sm103.cu — the fused attention forward with one Q tile per CTA
+// on GB300 (sm_103a): head dimension 256, and 128 under the causal mask.
 //
 // Same computation as the D = 64 / 128 kernel: out = softmax(scale·q·kᵀ +
 // causal mask)·v per (batch, head) with the row logsumexp, following the five
@@ -8,13 +8,19 @@
 // [S, S] scores never leave the chip (same page, "Why flash attention exists";
 // FlashAttention-2 blog, "FlashAttention-2 Optimizations" §1-§3).
 //
-// At D = 256 two Q tiles' O accumulators would fill TMEM on their own, so the
-// layout differs: one 128-row Q tile per CTA, K/V tiles of 64 rows, and two
-// 64-column S buffers so that the next S is computed while the softmax of the
-// current one runs.  Q is the A operand of every S product of the CTA: it is
-// put into TMEM once, so S = Q·Kᵀ is a TS product and shared memory only feeds
-// K and V.  TMEM columns: S_b [64b, 64b+64) (P_b, 16-bit, over its first 32),
-// Q [128, 256) (two 16-bit values per column), O [256, 512).
+// Layout: one 128-row Q tile per CTA, K/V tiles of BN rows (64 at D = 256,
+// 128 at D = 128), and two BN-column S buffers, so that the next S is computed
+// while the softmax of the current one runs: the softmaxes of one tile follow
+// each other back to back.  Q is the A operand of every S product of the CTA:
+// it is put into TMEM once, so S = Q·Kᵀ is a TS product and shared memory only
+// feeds K and V.  TMEM columns: S_b [BN·b, BN·b + BN) (P_b, 16-bit, over its
+// first BN/2), Q [2·BN, 2·BN + D/2) (two 16-bit values per column), O in the
+// last D.  The softmax computes its exponentials against the running
+// reference before the tile's max is known and redoes them only when the tile
+// moves the reference by more than 2^8.  At D = 256 two Q tiles' accumulators
+// would fill TMEM on their own; at D = 128 this layout runs the causal case
+// (the two-tile kernel stays faster when the reference moves often, as under a
+// peaked non-causal softmax).
 //
 // Roles (192 threads): warps 0-3 softmax / correction / epilogue, one thread
 // per query row (TMEM lane); warp 4 issues tcgen05.mma and owns TMEM; warp 5
@@ -30,19 +36,19 @@
 namespace ea {
 namespace {
 
-constexpr int kKvRows = 64;                      // rows of one K/V tile
 constexpr int kQRows = 128;                      // rows of the Q tile
 constexpr int kThreads1Q = 192;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units, as in the two-tile kernel
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
-constexpr int kChunkBytes = kKvRows * 128;       // one 64-column block of a K/V tile (8 KB)
 
-template <int D>
+// D: head dimension; BN: rows of one K/V tile
+template <int D, int BN>
 struct Layout1Q {
-  static constexpr int kTile = kKvRows * D * 2;  // one K/V tile
-  static constexpr int kKStages = (D == 256) ? 3 : 5;
-  static constexpr int kVStages = (D == 256) ? 3 : 5;
+  static constexpr int kChunkBytes = BN * 128;   // one 64-column block of a K/V tile
+  static constexpr int kTile = BN * D * 2;       // one K/V tile
+  static constexpr int kKStages = (kTile >= 32768) ? 3 : 5;
+  static constexpr int kVStages = (kTile >= 32768) ? 3 : 5;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKStages * kTile;
   static constexpr int kBarOff = kVOff + kVStages * kTile;
@@ -57,7 +63,8 @@ struct Layout1Q {
   static_assert(kAlloc <= 232448, "shared memory budget exceeded");
   // the epilogue stages O (128 rows x D 16-bit values) in the K ring
   static_assert(kKStages * kTile >= kQRows * D * 2, "O staging must fit the K ring");
-  static constexpr uint32_t kQCol = 128, kOCol = 256, kTmemCols = 512;
+  // TMEM: two S buffers of BN columns, then Q (D/2 columns), O in the last D
+  static constexpr uint32_t kTmemCols = 512, kQCol = 2 * BN, kOCol = kTmemCols - D;
   static_assert(kQCol + D / 2 <= kOCol && kOCol + D <= kTmemCols, "TMEM budget exceeded");
 };
 
@@ -65,9 +72,11 @@ enum : int { kSiteProdK = 0x3100, kSiteProdV = 0x3200, kSiteMmaQ = 0x3300, kSite
              kSiteMmaV = 0x3500, kSiteMmaP = 0x3600, kSiteSoftS = 0x3700, kSiteSoftPv = 0x3800,
              kSiteSoftO = 0x3900 };
 
-template <int D, bool CAUSAL, bool F16>
-__global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid_constant__ Fwd256Params p) {
-  using L = Layout1Q<D>;
+template <int D, int BN, bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid_constant__ Fwd1QParams p) {
+  using L = Layout1Q<D, BN>;
+  constexpr int kKvRows = BN;
+  constexpr int kChunkBytes = L::kChunkBytes;
   constexpr int kD = D;
   constexpr int kTile = L::kTile;
   constexpr int kKStages = L::kKStages, kVStages = L::kVStages;
@@ -84,11 +93,11 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Q tile i of slice bh, the tiles with the most keys first
-  const int level = blockIdx.x / p.BH;
-  const int bh = blockIdx.x - level * p.BH;
-  const int i = p.n_qt - 1 - level;
-  int nkv = CAUSAL ? 2 * i + 2 : p.n_kt;  // K/V tiles this Q tile meets
+  // Q tile i of slice bh, in the order of the grid schedule (schedule.h):
+  // heavy tiles by L2-sized groups of heads, then the light ones over all heads
+  int bh, i;
+  schedule_unit(p.sched, static_cast<int>(blockIdx.x), &bh, &i);
+  int nkv = CAUSAL ? (i + 1) * (kQRows / BN) : p.n_kt;  // K/V tiles this Q tile meets
   if (nkv > p.n_kt) nkv = p.n_kt;
 
   if (threadIdx.x == 0) {
@@ -157,27 +166,50 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
                                                 kSiteSoftS | (j & 0xff)));
       if (!ok) break;
       tc_fence_after_sync();
-      const uint32_t tS = tmem_base + lane_bits + 64 * b;
-      uint32_t s[2][32];
-      tmem_ld_32x32b_x32(tS, s[0]);
-      tmem_ld_32x32b_x32(tS + 32, s[1]);
+      const uint32_t tS = tmem_base + lane_bits + BN * b;
+      uint32_t s[BN / 32][32];
+#pragma unroll
+      for (int g = 0; g < BN / 32; ++g) tmem_ld_32x32b_x32(tS + 32 * g, s[g]);
       tmem_ld_wait();
-      reg_fence(s[0]);
-      reg_fence(s[1]);
+#pragma unroll
+      for (int g = 0; g < BN / 32; ++g) reg_fence(s[g]);
       // allowed key columns of this tile: 0 .. lim (causal: key <= query; key < S)
       int lim = p.S - 1 - j * kKvRows;
       if (CAUSAL) lim = min(lim, grow - j * kKvRows);
       if (!valid) lim = -1;
-      if (lim < 63) {
+      if (lim < BN - 1) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < BN; ++c)
           if (c > lim) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
-      for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(s[c >> 5][c & 31]));
+      for (int c = 0; c < BN; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(s[c >> 5][c & 31]));
       const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       const float m_tile = mx * sl2;
+      // exponentials against the current reference, computed before the
+      // reference update is known; redone only when the tile moves it
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      float2 rs2[4];
+      uint32_t pk[BN / 64][32];
+      auto exps = [&](float neg_m) {
+        const float2 nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) rs2[a] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < BN / 64; ++g)
+#pragma unroll
+          for (int e2 = 0; e2 < 32; ++e2) {
+            const int h = 2 * g + (e2 >> 4), e = (2 * e2) & 31;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[h][e]), __uint_as_float(s[h][e + 1])),
+                                        sl2x2, nm2);
+            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            rs2[e2 & 3] = __fadd2_rn(rs2[e2 & 3], make_float2(p0, p1));
+            pk[g][e2] = pack_x2<F16>(p0, p1);
+          }
+      };
+      const bool spec = m != -INFINITY;
+      if (spec) exps(-m);
       float alpha = 1.f;
       bool moved = false;
       if (m == -INFINITY) {
@@ -188,25 +220,19 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
         moved = true;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[32];
+      const bool any_moved = __any_sync(0xffffffffu, moved);  // every lane, no short-circuit
+      if (!spec || any_moved) exps(neg_m);
 #pragma unroll
-      for (int e2 = 0; e2 < 32; ++e2) {
-        const int h = e2 >> 4, e = (2 * e2) & 31;
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[h][e]), sl2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[h][e + 1]), sl2, neg_m));
-        rs0 += p0;
-        rs1 += p1;
-        pk[e2] = pack_x2<F16>(p0, p1);
-      }
-      tmem_st_32x32b_x32(tS, pk);
+      for (int g = 0; g < BN / 64; ++g) tmem_st_32x32b_x32(tS + 32 * g, pk[g]);
+      const float2 ra = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
+      const float rs0 = ra.x, rs1 = ra.y;
       const float rs = rs0 + rs1;
       const float pmax = ex2_approx(fmaf(mx, sl2, neg_m));
       l = l * alpha + rs;
       lq = lq * alpha + (rs + (round_to_x<F16>(pmax) - pmax));
       // correction: O of a row whose reference moved is rescaled before PV_j
       // accumulates into it; PV_{j-1} must have completed first
-      if (__any_sync(0xffffffffu, moved)) {
+      if (any_moved) {
         if (j > 0) {
           ok = __all_sync(0xffffffffu, wait_bounded(bar(kPvDone), (j - 1) & 1, ctl,
                                                     kSiteSoftPv | (j & 0xff)));
@@ -326,7 +352,7 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ts(tmem_base + 64 * (j & 1), tmem_base + kQCol + kk * 8, db + off, kIdescS,
+        mma_ts(tmem_base + BN * (j & 1), tmem_base + kQCol + kk * 8, db + off, kIdescS,
                kk > 0 ? 1u : 0u);
       }
       mma_commit(bar(kSFull + (j & 1)));
@@ -350,7 +376,7 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
         const uint64_t db = dv + (j % kVStages) * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < kKvRows / 16; ++kk)  // O += P_b · V_j, 16 keys per step
-          mma_ts(tmem_base + kOCol, tmem_base + 64 * b + kk * 8, db + kk * (2048 >> 4), kIdescO,
+          mma_ts(tmem_base + kOCol, tmem_base + BN * b + kk * 8, db + kk * (2048 >> 4), kIdescO,
                  (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(kPvDone));
         mma_commit(bar(kVEmpty + j % kVStages));
@@ -380,10 +406,10 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
   }
 }
 
-template <int D, bool CAUSAL, bool F16>
-cudaError_t launch_1q(const Fwd256Params& p, cudaStream_t stream) {
-  auto kern = attn_fwd_1q_kernel<D, CAUSAL, F16>;
-  constexpr int kAlloc = Layout1Q<D>::kAlloc;
+template <int D, int BN, bool CAUSAL, bool F16>
+cudaError_t launch_1q(const Fwd1QParams& p, cudaStream_t stream) {
+  auto kern = attn_fwd_1q_kernel<D, BN, CAUSAL, F16>;
+  constexpr int kAlloc = Layout1Q<D, BN>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -396,12 +422,14 @@ cudaError_t launch_1q(const Fwd256Params& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t fwd1q_launch(const Fwd256Params& p, int D, bool causal, bool f16, cudaStream_t stream) {
-  // The layout also works at D = 128 (parity-checked), but there one Q tile's
-  // softmax is not covered by its products: the two-tile kernel is faster.
+cudaError_t fwd1q_launch(const Fwd1QParams& p, int D, bool causal, bool f16, cudaStream_t stream) {
+  if (D == 128) {
+    if (f16) return causal ? launch_1q<128, 128, true, true>(p, stream) : launch_1q<128, 128, false, true>(p, stream);
+    return causal ? launch_1q<128, 128, true, false>(p, stream) : launch_1q<128, 128, false, false>(p, stream);
+  }
   if (D != 256) return cudaErrorInvalidValue;
-  if (f16) return causal ? launch_1q<256, true, true>(p, stream) : launch_1q<256, false, true>(p, stream);
-  return causal ? launch_1q<256, true, false>(p, stream) : launch_1q<256, false, false>(p, stream);
+  if (f16) return causal ? launch_1q<256, 64, true, true>(p, stream) : launch_1q<256, 64, false, true>(p, stream);
+  return causal ? launch_1q<256, 64, true, false>(p, stream) : launch_1q<256, 64, false, false>(p, stream);
 }
 
 }  // namespace ea
