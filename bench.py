@@ -48,7 +48,7 @@ KERNEL_SOURCES = ["exact_attention_68_gb300/csrc/attn_fwd_1q_sm103.cu",
 NCU_TRAFFIC_BYTES = {
     # B=1 H=32 S=16384 D=128 causal (attn_fwd_1q_kernel<128,128,true>):
     # 603,648,512 read + 117,861,888 written
-    "08bd8a0376c35a6a": 721510400,
+    "230d765411e56526": 721510400,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
