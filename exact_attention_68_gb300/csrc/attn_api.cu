@@ -73,7 +73,7 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
   if (B < 1 || H < 1 || S < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
+  if (D > 256 || D % 8 != 0) return ATTN_ERR_UNSUPPORTED;  // 16-byte rows for TMA
   // sizes: B·H and the grid fit int32, every byte count fits int64 (2^62)
   if (B > INT32_MAX || H > INT32_MAX || S > INT32_MAX) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = B * H;  // < 2^62, no overflow
@@ -81,7 +81,7 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
   const int64_t n_qt = (S + ea::kBlockM - 1) / ea::kBlockM;
   const int64_t n_units = (n_qt + ea::kQTilesPerUnit - 1) / ea::kQTilesPerUnit;
   if (BH * n_units > INT32_MAX) return ATTN_ERR_INVALID_ARG;
-  if (D == 256 && BH * n_qt > INT32_MAX) return ATTN_ERR_INVALID_ARG;  // one CTA per Q tile
+  if (BH * n_qt > INT32_MAX) return ATTN_ERR_INVALID_ARG;  // one CTA per Q tile
   if (BH > (int64_t(1) << 62) / (S * D * 2)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15u)
@@ -162,10 +162,15 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
                                  float scale, int causal, bool f16, uint64_t timeout_ns,
                                  int* status, cudaStream_t stream) {
   const int64_t BH = B * H;
-  // One Q tile per CTA for D = 256, and for causal D = 128 (measured faster
+  // The kernels exist for 64, 128 and 256 columns; another head dimension
+  // runs on the next one up.  The tensor maps carry the real column count,
+  // so TMA loads read zeros past it and stores leave those columns out; the
+  // zero columns add nothing to q·kᵀ and give zero output columns.
+  const int dk = kernel_head_dim(D);
+  // One Q tile per CTA for 256 columns, and for causal 128 (measured faster
   // there); the two-tile kernel otherwise.
-  if (D == 256 || (D == 128 && causal != 0)) {
-    const int bn = D == 256 ? 64 : 128;  // rows of one K/V tile
+  if (dk == 256 || (dk == 128 && causal != 0)) {
+    const int bn = dk == 256 ? 64 : 128;  // rows of one K/V tile
     Fwd1QParams p;
     std::memset(&p, 0, sizeof(p));
     if (!encode_bhsd_16bit(&p.tm_k, k, BH, S, D, bn, f16) ||
@@ -177,6 +182,7 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
     p.status = status;
     p.BH = static_cast<int>(BH);
     p.S = static_cast<int>(S);
+    p.d_cols = static_cast<int>(D);
     p.n_qt = static_cast<int>((S + 127) / 128);
     p.n_kt = static_cast<int>((S + bn - 1) / bn);
     int dev1 = 0, sms1 = 0;
@@ -186,7 +192,7 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
     p.sched = plan_schedule(BH, p.n_qt, S, D, causal != 0, kL2GroupBytes, sms1);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.timeout_ns = timeout_ns;
-    const cudaError_t e = fwd1q_launch(p, static_cast<int>(D), causal != 0, f16, stream);
+    const cudaError_t e = fwd1q_launch(p, dk, causal != 0, f16, stream);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       return cuda_failure(static_cast<int>(e));
@@ -214,7 +220,7 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
   p.sched = plan_schedule(BH, p.n_units, S, D, causal != 0, kL2GroupBytes, sms);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout_ns;
-  e = fwd_launch(p, static_cast<int>(D), causal != 0, f16, stream);
+  e = fwd_launch(p, dk, causal != 0, f16, stream);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return cuda_failure(static_cast<int>(e));
@@ -326,7 +332,8 @@ const char* attn_status_string(attn_status_t status) {
     case ATTN_OK: return "ok";
     case ATTN_ERR_INVALID_ARG: return "invalid argument";
     case ATTN_ERR_UNSUPPORTED:
-      return "unsupported (head_dim must be 64, 128 or, forward only, 256; device must be sm_103)";
+      return "unsupported (head_dim must be a multiple of 8, at most 256 (128 for the backward); "
+             "device must be sm_103)";
     case ATTN_ERR_MISALIGNED: return "misaligned pointer (q/k/v/out need 16 bytes, lse 4 bytes)";
     case ATTN_ERR_CUDA: return "CUDA call failed";
     case ATTN_ERR_TIMEOUT: return "an in-kernel wait ran out of time";

@@ -21,15 +21,17 @@ struct BwdParams {
   CUtensorMap tm_dq;  // dq, box 64 x 32 rows (one warp's rows)
   CUtensorMap tm_dk;  // dk, same
   CUtensorMap tm_dv;  // dv, same
-  const uint16_t* q;     // 16-bit [B·H, S, D]: rows read into TMEM by the dq kernel
-  const uint16_t* k;     // 16-bit [B·H, S, D]: rows read into TMEM by the dk/dv kernel
-  const uint16_t* v;     // 16-bit [B·H, S, D]: rows read into TMEM by the dk/dv kernel
-  const uint16_t* out;   // 16-bit [B·H, S, D]: forward output (rows read for delta)
-  const uint16_t* dout;  // 16-bit [B·H, S, D]
+  const uint16_t* q;     // 16-bit [B·H, S, d_cols]: rows read into TMEM by the dq kernel
+  const uint16_t* k;     // 16-bit [B·H, S, d_cols]: rows read into TMEM by the dk/dv kernel
+  const uint16_t* v;     // 16-bit [B·H, S, d_cols]: rows read into TMEM by the dk/dv kernel
+  const uint16_t* out;   // 16-bit [B·H, S, d_cols]: forward output (rows read for delta)
+  const uint16_t* dout;  // 16-bit [B·H, S, d_cols]
   const float* lse;      // [B·H, S]: natural-log logsumexp saved by the forward
   float* delta;          // [B·H, S]: rowsum(dout ⊙ out), written by the dq kernel
   int* status;           // device status word pair (error bits, first wait site)
   int BH, S;
+  int d_cols;            // the tensors' head dimension (<= the kernel's D, a multiple
+                         // of 8); the kernel's columns past it are zero
   int n_t;               // ceil(S / 128): tiles along the sequence
   float scale;           // softmax scale
   float scale_log2;      // scale · log2(e)

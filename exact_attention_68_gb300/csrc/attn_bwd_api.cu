@@ -24,7 +24,7 @@ attn_status_t validate_bwd(const void* q, const void* k, const void* v, const vo
   // shapes, scale, mask flag, q/k/v/out/lse pointers and alignment
   attn_status_t s = ea::validate_args(q, k, v, out, lse, B, H, S, D, scale, causal);
   if (s != ATTN_OK) return s;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;  // the backward: D = 64, 128
+  if (D > 128) return ATTN_ERR_UNSUPPORTED;  // the backward: D <= 128
   if (!dout || !dq || !dk || !dv || !delta) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u)
@@ -83,12 +83,15 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
   p.status = status;
   p.BH = static_cast<int>(BH);
   p.S = static_cast<int>(S);
+  p.d_cols = static_cast<int>(D);
   p.n_t = static_cast<int>((S + 127) / 128);
   if (static_cast<int64_t>(p.BH) * p.n_t > INT32_MAX) return ATTN_ERR_INVALID_ARG;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = wait_timeout_ns;
-  const cudaError_t e = ea::bwd_launch(p, static_cast<int>(D), causal != 0, f16, stream);
+  // kernels of 64 or 128 columns; the tensor maps carry the real column
+  // count (zeros read past it, those columns never stored)
+  const cudaError_t e = ea::bwd_launch(p, ea::kernel_head_dim(D), causal != 0, f16, stream);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return ea::cuda_failure(static_cast<int>(e));

@@ -237,14 +237,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       constexpr int kU = D / 16;  // 16-byte groups in half a row
       uint32_t qw[4 * kU], dw[4 * kU];
       if (valid) {
-        const int64_t base = ((int64_t)bh * p.S + grow) * D;
-        const uint4* q4 = reinterpret_cast<const uint4*>(p.q + base) + g * kU;
-        const uint4* o4 = reinterpret_cast<const uint4*>(p.out + base) + g * kU;
-        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + base) + g * kU;
+        // columns past d_cols hold zero
+        const int64_t base = ((int64_t)bh * p.S + grow) * p.d_cols + g * (D / 2);
+        const int lim = p.d_cols - g * (D / 2);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          const uint4 qv = __ldg(q4 + u), dv = __ldg(d4 + u);
-          part += dot8<F16>(__ldg(o4 + u), dv);
+          const bool in = 8 * u < lim;
+          const uint4 qv = in ? __ldg(reinterpret_cast<const uint4*>(p.q + base) + u) : z;
+          const uint4 dv = in ? __ldg(reinterpret_cast<const uint4*>(p.dout + base) + u) : z;
+          const uint4 ov = in ? __ldg(reinterpret_cast<const uint4*>(p.out + base) + u) : z;
+          part += dot8<F16>(ov, dv);
           qw[4 * u] = qv.x, qw[4 * u + 1] = qv.y, qw[4 * u + 2] = qv.z, qw[4 * u + 3] = qv.w;
           dw[4 * u] = dv.x, dw[4 * u + 1] = dv.y, dw[4 * u + 2] = dv.z, dw[4 * u + 3] = dv.w;
         }
@@ -577,12 +580,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       constexpr int kU = D / 16;  // 16-byte groups in half a row
       uint32_t kw[4 * kU], vw[4 * kU];
       if (gk < p.S) {
-        const int64_t base = ((int64_t)bh * p.S + gk) * D;
-        const uint4* k4 = reinterpret_cast<const uint4*>(p.k + base) + g * kU;
-        const uint4* v4 = reinterpret_cast<const uint4*>(p.v + base) + g * kU;
+        // columns past d_cols hold zero
+        const int64_t base = ((int64_t)bh * p.S + gk) * p.d_cols + g * (D / 2);
+        const int lim = p.d_cols - g * (D / 2);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          const uint4 kv = __ldg(k4 + u), vv = __ldg(v4 + u);
+          const bool in = 8 * u < lim;
+          const uint4 kv = in ? __ldg(reinterpret_cast<const uint4*>(p.k + base) + u) : z;
+          const uint4 vv = in ? __ldg(reinterpret_cast<const uint4*>(p.v + base) + u) : z;
           kw[4 * u] = kv.x, kw[4 * u + 1] = kv.y, kw[4 * u + 2] = kv.z, kw[4 * u + 3] = kv.w;
           vw[4 * u] = vv.x, vw[4 * u + 1] = vv.y, vw[4 * u + 2] = vv.z, vw[4 * u + 3] = vv.w;
         }

@@ -45,10 +45,12 @@ struct Fwd1QParams {
   CUtensorMap tm_k;    // k as (D, S, B·H), box 64 x BN rows, 128-byte swizzle
   CUtensorMap tm_v;    // v, same box
   CUtensorMap tm_o;    // out, box 64 x 32 rows
-  const uint16_t* q;   // 16-bit [B·H, S, D]: rows read into TMEM
+  const uint16_t* q;   // 16-bit [B·H, S, d_cols]: rows read into TMEM
   float* lse;          // [B·H, S]
   int* status;
   int BH, S;
+  int d_cols;          // the tensors' head dimension (<= D, a multiple of 8); the
+                       // kernel's columns past it are zero and never stored
   int n_qt;            // ceil(S / 128)
   int n_kt;            // ceil(S / BN)
   UnitSchedule sched;  // CTA index -> (b·H + h, Q tile): a unit is one Q tile here

@@ -139,14 +139,17 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
     const uint32_t tO = tmem_base + lane_bits + kOCol;
     {
       // this row of Q into TMEM, 32 columns (64 values) per store
-      const int64_t qrow = valid ? (int64_t)bh * p.S + grow : 0;  // rows past S load nothing
-      const uint4* q4 = reinterpret_cast<const uint4*>(p.q + qrow * kD);
+      // (rows past S and columns past d_cols load nothing and hold zero)
+      const int64_t qrow = valid ? (int64_t)bh * p.S + grow : 0;
+      const uint16_t* qr = p.q + qrow * p.d_cols;
 #pragma unroll
       for (int c = 0; c < kD / 64; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint4 x = valid ? __ldg(q4 + 8 * c + u) : make_uint4(0u, 0u, 0u, 0u);
+          const int col = 64 * c + 8 * u;
+          const uint4 x = valid && col < p.d_cols ? __ldg(reinterpret_cast<const uint4*>(qr + col))
+                                                  : make_uint4(0u, 0u, 0u, 0u);
           w[4 * u] = x.x, w[4 * u + 1] = x.y, w[4 * u + 2] = x.z, w[4 * u + 3] = x.w;
         }
         tmem_st_32x32b_x32(tmem_base + lane_bits + kQCol + 32 * c, w);
@@ -285,8 +288,9 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
       if (lane == 0) {
 #pragma unroll
         for (int c = 0; c < kD / 64; ++c)
-          tma_store_3d(&p.tm_o, sb + kKOff + c * (kQRows * 128) + warp * 32 * 128, c * 64,
-                       i * kQRows + warp * 32, bh);
+          if (64 * c < p.d_cols)  // a chunk wholly past the tensor's columns is not stored
+            tma_store_3d(&p.tm_o, sb + kKOff + c * (kQRows * 128) + warp * 32 * 128, c * 64,
+                         i * kQRows + warp * 32, bh);
         tma_store_commit();
       }
       if (valid) p.lse[(int64_t)bh * p.S + grow] = (m + __log2f(l)) * kLn2;

@@ -42,6 +42,10 @@ inline cudaError_t current_device_bound(int* dev) {
   return e;
 }
 
+// Columns of the kernel that runs a head dimension D (a multiple of 8, at
+// most 256): the smallest of 64, 128, 256 that holds D.
+inline int kernel_head_dim(int64_t D) { return D <= 64 ? 64 : D <= 128 ? 128 : 256; }
+
 // True if the byte ranges [a, a+na) and [b, b+nb) intersect.
 inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);

@@ -57,7 +57,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, size < 1, overflow, scale not finite and > 0, causal not 0/1, aliasing */
-  ATTN_ERR_UNSUPPORTED = 2,  /* head_dim other than 64, 128 (or 256 for the forward), or no sm_103a device */
+  ATTN_ERR_UNSUPPORTED = 2,  /* head_dim not a multiple of 8 or above 256 (128 for the backward), or no sm_103a device */
   ATTN_ERR_MISALIGNED = 3,   /* a pointer not 16-byte aligned */
   ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, tensor-map encode) */
   ATTN_ERR_TIMEOUT = 5       /* a bounded in-kernel wait ran out (reported by attn_device_status) */
@@ -79,7 +79,10 @@ typedef enum {
  *   out      device pointer, bf16 [B, H, S, D] contiguous, 16-byte aligned (written)
  *   lse      device pointer, fp32 [B, H, S] contiguous, 4-byte aligned (written)
  *   B, H, S  batch, heads, sequence length; each >= 1, B·H < 2^31, S < 2^31
- *   D        head dimension: 64, 128 or 256 (the backward: 64 or 128)
+ *   D        head dimension: a multiple of 8, at most 256 (the backward: at most
+ *            128).  64, 128 and 256 run on kernels of that width; any other D
+ *            runs on the next width up with the columns past D read as zero
+ *            (exact: they add nothing to q·kᵀ), so it costs what that width costs
  *   scale    multiplier of q·kᵀ (normally 1/sqrt(D)); must be finite and > 0
  *   causal   1: mask key j > query i; 0: no mask
  *   stream   CUDA stream the work is enqueued on (0 = legacy default stream)

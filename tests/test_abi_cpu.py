@@ -62,9 +62,10 @@ def _call(lib, q=A, k=A + T, v=A + 2 * T, out=A + 3 * T, lse=A + 4 * T,
     (dict(H=-1), binding.ATTN_ERR_INVALID_ARG),
     (dict(S=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(D=0), binding.ATTN_ERR_INVALID_ARG),
-    (dict(D=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(D=100), binding.ATTN_ERR_UNSUPPORTED),   # rows not a multiple of 16 bytes
+    (dict(D=4), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(D=264), binding.ATTN_ERR_UNSUPPORTED),
     (dict(D=512), binding.ATTN_ERR_UNSUPPORTED),
-    (dict(D=32), binding.ATTN_ERR_UNSUPPORTED),
     (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
     (dict(scale=-0.5), binding.ATTN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), binding.ATTN_ERR_INVALID_ARG),
@@ -105,7 +106,7 @@ def test_noalloc_validates_before_touching_the_gpu(lib):
     bad[0] = 0
     assert lib.attn_fwd_noalloc(*bad, 1, None) == binding.ATTN_ERR_INVALID_ARG
     bad = list(args)
-    bad[8] = 80
+    bad[8] = 84  # not a multiple of 8
     assert lib.attn_fwd_noalloc(*bad, 1, None) == binding.ATTN_ERR_UNSUPPORTED
 
 
@@ -125,8 +126,9 @@ def _bwd(lib, q=A, k=A + T, v=A + 2 * T, out=A + 3 * T, lse=A + 4 * T, dout=A + 
     (dict(dv=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(delta=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(S=0), binding.ATTN_ERR_INVALID_ARG),
-    (dict(D=96), binding.ATTN_ERR_UNSUPPORTED),
-    (dict(D=256), binding.ATTN_ERR_UNSUPPORTED),   # the forward has D=256, the backward not
+    (dict(D=100), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(D=136), binding.ATTN_ERR_UNSUPPORTED),   # the forward goes to 256, the backward to 128
+    (dict(D=256), binding.ATTN_ERR_UNSUPPORTED),
     (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
     (dict(causal=3), binding.ATTN_ERR_INVALID_ARG),
     (dict(dout=A + 5 * T + 8), binding.ATTN_ERR_MISALIGNED),
@@ -154,7 +156,7 @@ def test_ex_entry_points_validate_dtype_first(lib):
     assert lib.attn_fwd_ex(*fwd, 2, binding.ATTN_DEFAULT_WAIT_TIMEOUT_NS, None) == binding.ATTN_ERR_INVALID_ARG
     assert lib.attn_fwd_ex(*fwd, -1, binding.ATTN_DEFAULT_WAIT_TIMEOUT_NS, None) == binding.ATTN_ERR_INVALID_ARG
     bad = list(fwd)
-    bad[8] = 96
+    bad[8] = 260
     assert lib.attn_fwd_ex(*bad, binding.ATTN_F16, 0, None) == binding.ATTN_ERR_UNSUPPORTED
     bwd = [A, A + T, A + 2 * T, A + 3 * T, A + 4 * T, A + 5 * T, A + 6 * T, A + 7 * T, A + 8 * T,
            A + 9 * T, 1, 2, 128, 64, 0.125, 1]

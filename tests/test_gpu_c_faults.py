@@ -46,7 +46,7 @@ def test_argument_errors_on_gpu_launch_nothing(cuda_device):
     lse = torch.full((1, 1, 128), 7.0, device="cuda:0")
     lib = binding.load_library()
     rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                      1, 1, 128, 96, 0.1, 1, None)
+                      1, 1, 128, 100, 0.1, 1, None)
     assert rc == binding.ATTN_ERR_UNSUPPORTED
     rc = lib.attn_fwd(q.data_ptr() + 2, k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                       1, 1, 128, 64, 0.1, 1, None)
