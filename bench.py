@@ -160,20 +160,42 @@ def barrier(world: int):
         dist.barrier()
 
 
+def parity_of_outputs(checked, out, lse):
+    """The benchmark's outputs (those of its last end-to-end step, which the
+    tests show equal the device path's bit for bit) on the rows the CPU
+    baseline computed, against the oracle's values, with the parity tests' bars."""
+    idx = np.concatenate([c[0] for c in checked])
+    ro = np.concatenate([c[1] for c in checked])
+    rl = np.concatenate([c[2] for c in checked])
+    b, h, r = (torch.from_numpy(idx[:, n]) for n in range(3))
+    og = out.cpu()[b, h, r].double().numpy()
+    lg = lse.cpu()[b, h, r].double().numpy()
+    err, lerr = np.abs(og - ro), np.abs(lg - rl)
+    res = {"rows": int(idx.shape[0]), "out_max_err": float(err.max()),
+           "out_mean_err": float(err.mean()), "lse_max_err": float(lerr.max()),
+           "bars": {"out_max": 2e-2, "out_mean": 2e-3, "lse_max": 1e-3}}
+    res["pass"] = bool(res["out_max_err"] <= 2e-2 and res["out_mean_err"] <= 2e-3
+                       and res["lse_max_err"] <= 1e-3 and np.isfinite(og).all())
+    return res
+
+
 def as_numpy(q, k, v):
     """bf16 tensors -> float32 numpy arrays (exact), converted once per run."""
     return tuple(x.float().numpy() for x in (q, k, v))
 
 
-def oracle_rows_sample(qn, kn, vn, scale, causal, rows_per_head, heads, budget_s):
-    """Time the fp64 oracle (row form) on evenly spaced rows; return (tflops, rows, secs)."""
+def oracle_rows_sample(qn, kn, vn, scale, causal, rows_per_head, heads, budget_s, results=None):
+    """Time the fp64 oracle (row form) on evenly spaced rows; return (tflops, rows, secs).
+    If `results` is a list, each head's (index, out rows, lse rows) is appended to it."""
     from oracle import attention_rows  # CPU baseline leg only
     B, H, S, D = qn.shape
     rows = np.linspace(0, S - 1, rows_per_head).round().astype(np.int64)
     done, flops, t0 = 0, 0, time.perf_counter()
     for h in heads:
         idx = np.stack([np.zeros_like(rows), np.full_like(rows, h), rows], 1)
-        attention_rows(qn, kn, vn, scale, causal, idx)
+        ro, rl = attention_rows(qn, kn, vn, scale, causal, idx)
+        if results is not None:
+            results.append((idx, ro, rl))
         done += len(rows)
         n_keys = (rows + 1) if causal else np.full_like(rows, S)
         flops += int(4 * D * n_keys.sum())
@@ -391,13 +413,15 @@ def run_ours(args, world, rank, local):
         extra["backward"] = bwd
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
+        checked = []
         tf, n_rows, secs = oracle_rows_sample(*as_numpy(q_h, k_h, v_h), scale, w.causal, 256,
-                                              list(range(w.H)), args.cpu_budget)
+                                              list(range(w.H)), args.cpu_budget, checked)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
                "kind": "oracle", "blas_threads": blas_threads(),
                "full_problem_s_extrapolated": flops / (tf * 1e12),
                "sample": f"{n_rows} query rows (256 evenly spaced per head, heads in order) of the "
                          f"{w.about} workload, oracle row form in fp64 numpy, {secs:.1f} s"}
+        extra["parity"] = parity_of_outputs(checked, out_h, lse_h)
     if rank != 0:
         return
     nb = w.B * w.H * w.S * w.D * 2

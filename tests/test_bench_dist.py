@@ -50,3 +50,26 @@ def test_two_gloo_ranks_take_the_max_time():
 def test_single_rank_needs_no_process_group():
     import bench
     assert bench.reduce_max(3.5, 1, "cpu") == 3.5
+
+
+def test_bench_parity_block_uses_the_oracle_rows():
+    """The bench line's parity block: oracle rows against the outputs on the
+    same (b, h, row) triples; a planted error in one output row fails it."""
+    import numpy as np
+    import torch
+    import bench
+    from exact_attention_68_gb300.workloads import make_qkv
+    from oracle import attention_fwd
+    q, k, v = make_qkv((1, 2, 64, 16), seed=3)
+    qn, kn, vn = bench.as_numpy(q, k, v)
+    checked = []
+    bench.oracle_rows_sample(qn, kn, vn, 0.25, True, 16, [0, 1], 1e9, checked)
+    ro, rl = attention_fwd(qn.astype(np.float64), kn.astype(np.float64), vn.astype(np.float64),
+                           0.25, True)
+    out = torch.from_numpy(ro).to(torch.bfloat16)
+    lse = torch.from_numpy(rl).float()
+    res = bench.parity_of_outputs(checked, out, lse)
+    assert res["rows"] == 32 and res["pass"], res
+    bad = out.clone()
+    bad[0, 1, 63, 5] += 0.5  # the last row of head 1 is one of the sampled rows
+    assert not bench.parity_of_outputs(checked, bad, lse)["pass"]
