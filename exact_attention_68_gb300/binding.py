@@ -20,10 +20,11 @@ from .build import LIB_PATH
 __all__ = ["AttnError", "load_library", "attn_fwd", "attn_fwd_bounded", "attn_fwd_staged",
            "attn_fwd_noalloc", "attn_bwd", "attn_bwd_bounded", "attention", "device_status",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
-           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_F16", "EXPORTED_SYMBOLS"]
+           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_ERR_DEVICE_CHECK", "ATTN_BF16", "ATTN_F16", "EXPORTED_SYMBOLS"]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
 ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 3, 4, 5
+ATTN_ERR_DEVICE_CHECK = 6
 ATTN_BF16, ATTN_F16 = 0, 1
 ATTN_DEFAULT_WAIT_TIMEOUT_NS = 2_000_000_000
 

@@ -18,6 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIBDIR, "libattn_sm103.so")
+DEBUG_LIB_PATH = os.path.join(LIBDIR, "libattn_sm103_debug.so")
 UNIT_SRC = os.path.join(ROOT, "tests", "cuda", "umma_unit.cu")
 UNIT_LIB = os.path.join(ROOT, "tests", "cuda", "libumma_unit.so")
 SCHED_SRC = os.path.join(ROOT, "tests", "cuda", "sched_check.cpp")
@@ -72,6 +73,18 @@ def build_library(force: bool = False, verbose: bool = False, extra=()) -> str:
         _run([_nvcc(), *ARCH, *FLAGS, *extra, "-o", tmp, *_sources()], verbose)
         os.replace(tmp, LIB_PATH)
     return LIB_PATH
+
+
+def build_debug_library(force: bool = False, verbose: bool = False) -> str:
+    """Build the debug variant of the library (-DATTN_DEBUG: every kernel checks
+    its index arithmetic before each memory access and reports a failed check
+    as ATTN_ERR_DEVICE_CHECK instead of making the access); return its path."""
+    os.makedirs(LIBDIR, exist_ok=True)
+    if force or _stale(DEBUG_LIB_PATH, _deps()):
+        tmp = DEBUG_LIB_PATH + ".tmp"
+        _run([_nvcc(), *ARCH, *FLAGS, "-DATTN_DEBUG", "-o", tmp, *_sources()], verbose)
+        os.replace(tmp, DEBUG_LIB_PATH)
+    return DEBUG_LIB_PATH
 
 
 def build_unit_library(force: bool = False, verbose: bool = False) -> str:

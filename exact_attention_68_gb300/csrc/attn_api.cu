@@ -211,6 +211,7 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
   p.B = static_cast<int>(B);
   p.H = static_cast<int>(H);
   p.S = static_cast<int>(S);
+  p.d_cols = static_cast<int>(D);
   p.n_qt = static_cast<int>((S + kBlockM - 1) / kBlockM);
   p.n_units = (p.n_qt + kQTilesPerUnit - 1) / kQTilesPerUnit;
   int dev = 0, sms = 0;
@@ -324,7 +325,7 @@ attn_status_t attn_device_status(cudaStream_t stream) {
     return ATTN_ERR_CUDA;
   if (h[0] == 0) return ATTN_OK;
   if (cudaMemset(st->status, 0, sizeof(h)) != cudaSuccess) return ATTN_ERR_CUDA;
-  return ATTN_ERR_TIMEOUT;
+  return ea::status_of_words(h[0]);
 }
 
 const char* attn_status_string(attn_status_t status) {
@@ -337,6 +338,8 @@ const char* attn_status_string(attn_status_t status) {
     case ATTN_ERR_MISALIGNED: return "misaligned pointer (q/k/v/out need 16 bytes, lse 4 bytes)";
     case ATTN_ERR_CUDA: return "CUDA call failed";
     case ATTN_ERR_TIMEOUT: return "an in-kernel wait ran out of time";
+    case ATTN_ERR_DEVICE_CHECK:
+      return "an in-kernel index check failed (debug build); the access was skipped";
   }
   return "unknown status";
 }

@@ -64,6 +64,9 @@ enum : int {
   kSiteKvProducer = 0x2100, kSiteKvMmaKV = 0x2200, kSiteKvMmaQ = 0x2300, kSiteKvMmaP = 0x2400,
   kSiteKvElemS = 0x2500, kSiteKvElemO = 0x2600
 };
+// debug-check sites (-DATTN_DEBUG)
+enum : int { kChkAccTmem = 0x5201, kChkStage, kChkStore, kChkRowLoad, kChkRowTmem, kChkSTmem,
+             kChkStat, kChkLoadA, kChkLoadB, kChkMmaA, kChkMmaB };
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
@@ -110,7 +113,8 @@ __device__ __forceinline__ void st_shared_f32x2(uint32_t addr, float a, float b)
 template <bool F16>
 __device__ __forceinline__ void store_chunk(uint32_t tmem_col, uint32_t chunk_base, int row,
                                             float mul, const CUtensorMap* map, int x, int y0,
-                                            int z, int wq, int lane) {
+                                            int z, int wq, int lane, const DbgBounds& dbb) {
+  if (!dbg_warp(dbg_tmem(dbb, tmem_col, 64, wq, kChkAccTmem))) return;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     uint32_t o[32];
@@ -126,12 +130,16 @@ __device__ __forceinline__ void store_chunk(uint32_t tmem_col, uint32_t chunk_ba
       for (int e = 0; e < 4; ++e)
         w[e] = pack_x2<F16>(__uint_as_float(o[q4 * 8 + 2 * e]) * mul,
                            __uint_as_float(o[q4 * 8 + 2 * e + 1]) * mul);
-      st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+      if (dbg_smem(dbb, addr, 16, 16, kChkStage)) st_shared_v4(addr, w[0], w[1], w[2], w[3]);
     }
   }
   fence_proxy_async_smem();
   __syncwarp();
-  if (lane == 0) tma_store_3d(map, chunk_base + wq * 32 * 128, x, y0 + wq * 32, z);
+  // the warp's 32 rows, if any of them is inside the tensor
+  const int y = y0 + wq * 32;
+  const uint32_t src = chunk_base + wq * 32 * 128;
+  if (lane == 0 && y < dbb.rows && dbg_tma(dbb, src, 32 * 128, x, y, z, true, kChkStore))
+    tma_store_3d(map, src, x, y, z);
 }
 
 // ============================================================== dq kernel
@@ -179,6 +187,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
   const int lane = threadIdx.x & 31;
 
   // Q tile i of slice bh; the tiles with the most K/V tiles first
+  const DbgBounds dbb{p.status, sb, smem_u32(smem_raw) + static_cast<uint32_t>(L::kAlloc), p.S,
+                      p.d_cols, p.BH};
   const int level = blockIdx.x / p.BH;
   const int bh = blockIdx.x - level * p.BH;
   const int i = p.n_t - 1 - level;
@@ -243,7 +253,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          const bool in = 8 * u < lim;
+          const bool in = 8 * u < lim && dbg_row(dbb, bh, grow, g * (D / 2) + 8 * u, 8, kChkRowLoad);
           const uint4 qv = in ? __ldg(reinterpret_cast<const uint4*>(p.q + base) + u) : z;
           const uint4 dv = in ? __ldg(reinterpret_cast<const uint4*>(p.dout + base) + u) : z;
           const uint4 ov = in ? __ldg(reinterpret_cast<const uint4*>(p.out + base) + u) : z;
@@ -255,8 +265,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
 #pragma unroll
         for (int w = 0; w < 4 * kU; ++w) qw[w] = dw[w] = 0u;
       }
-      tmem_st_words(tmem_base + lane_bits + L::kQCol + g * (D / 4), qw);
-      tmem_st_words(tmem_base + lane_bits + L::kDoCol + g * (D / 4), dw);
+      if (dbg_warp(dbg_tmem(dbb, tmem_base + lane_bits + L::kQCol + g * (D / 4), D / 4, warp,
+                            kChkRowTmem) &&
+                   dbg_tmem(dbb, tmem_base + lane_bits + L::kDoCol + g * (D / 4), D / 4, warp,
+                            kChkRowTmem))) {
+        tmem_st_words(tmem_base + lane_bits + L::kQCol + g * (D / 4), qw);
+        tmem_st_words(tmem_base + lane_bits + L::kDoCol + g * (D / 4), dw);
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kQFull));
@@ -265,8 +280,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     named_bar_sync(1, 256);
     const float delta = ld_shared_f32(sb + L::kPartOff + 4 * row) +
                         ld_shared_f32(sb + L::kPartOff + 4 * (kTileRows + row));
-    if (g == 0 && valid) p.delta[(int64_t)bh * p.S + grow] = delta;
-    const float lse2 = valid ? p.lse[(int64_t)bh * p.S + grow] * kLog2e : 0.f;
+    const bool row_ok = valid && dbg_row(dbb, bh, grow, 0, 0, kChkRowLoad);
+    if (g == 0 && row_ok) p.delta[(int64_t)bh * p.S + grow] = delta;
+    const float lse2 = row_ok ? p.lse[(int64_t)bh * p.S + grow] * kLog2e : 0.f;
     const float sl2 = p.scale_log2;
 
     bool ok = true;
@@ -276,6 +292,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       if (!ok) break;
       tc_fence_after_sync();
       uint32_t s[2][32], dp[2][32];
+      if (!dbg_warp(dbg_tmem(dbb, tS, 64, warp, kChkSTmem) && dbg_tmem(dbb, tP, 64, warp, kChkSTmem))) {
+        ok = false;
+        break;
+      }
       tmem_ld_32x32b_x32(tS, s[0]);
       tmem_ld_32x32b_x32(tS + 32, s[1]);
       tmem_ld_32x32b_x32(tP, dp[0]);
@@ -321,7 +341,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       tc_fence_after_sync();
       for (int c = g; c < L::kChunks; c += 2)
         store_chunk<F16>(tQ + c * 64, sb + L::kKOff + c * kChunkBytes, row, p.scale, &p.tm_dq, c * 64,
-                    i * kTileRows, bh, wq, lane);
+                         i * kTileRows, bh, wq, lane, dbb);
       if (lane == 0) {
         tma_store_commit();
         tma_store_wait_all();
@@ -344,9 +364,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
         if (!ok) break;
         mbar_arrive_expect_tx(bar(L::kKFull + ks), L::kTile);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sb + L::kKOff + ks * L::kTile + c * kChunkBytes, &p.tm_k, bar(L::kKFull + ks),
-                      c * 64, j * kTileRows, bh, pol_kv);
+        for (int c = 0; c < L::kChunks; ++c) {
+          // a skipped copy leaves the stage's transaction count short: the
+          // consumer's bounded wait then ends the kernel
+          const uint32_t dst = sb + L::kKOff + ks * L::kTile + c * kChunkBytes;
+          if (dbg_tma(dbb, dst, kChunkBytes, c * 64, j * kTileRows, bh, false, kChkLoadA))
+            tma_load_3d(dst, &p.tm_k, bar(L::kKFull + ks), c * 64, j * kTileRows, bh, pol_kv);
+        }
         k_issued = j + 1;
         const int vs = j % L::kVStages;
         ok = wait_bounded(bar(L::kVEmpty + vs), ((j / L::kVStages) & 1) ^ 1, ctl,
@@ -354,9 +378,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
         if (!ok) break;
         mbar_arrive_expect_tx(bar(L::kVFull + vs), L::kTile);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sb + L::kVOff + vs * L::kTile + c * kChunkBytes, &p.tm_v, bar(L::kVFull + vs),
-                      c * 64, j * kTileRows, bh, pol_kv);
+        for (int c = 0; c < L::kChunks; ++c) {
+          const uint32_t dst = sb + L::kVOff + vs * L::kTile + c * kChunkBytes;
+          if (dbg_tma(dbb, dst, kChunkBytes, c * 64, j * kTileRows, bh, false, kChkLoadB))
+            tma_load_3d(dst, &p.tm_v, bar(L::kVFull + vs), c * 64, j * kTileRows, bh, pol_kv);
+        }
         v_issued = j + 1;
       }
       if (ok) {
@@ -391,6 +417,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     // SP(j, h): S_h = Q · K_j[64h, 64h+64)ᵀ and dP_h = dO · V_j[64h, 64h+64)ᵀ,
     // A (Q, dO) from TMEM, 8 columns per K step of 16
     auto issue_sp = [&](int ks, int vs, int h) {
+      if (!dbg_smem(dbb, sb + L::kKOff + ks * L::kTile, L::kTile, 1024, kChkMmaA) ||
+          !dbg_smem(dbb, sb + L::kVOff + vs * L::kTile, L::kTile, 1024, kChkMmaB))
+        return;  // S_h never completes: the elementwise warps' bounded wait ends the kernel
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
@@ -532,6 +561,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
 
   // K/V tile j of slice bh; under the mask tile j meets Q tiles j .. n_t-1,
   // so ascending j is heaviest first
+  const DbgBounds dbb{p.status, sb, smem_u32(smem_raw) + static_cast<uint32_t>(L::kAlloc), p.S,
+                      p.d_cols, p.BH};
   const int j = blockIdx.x / p.BH;
   const int bh = blockIdx.x - j * p.BH;
   const int i0 = CAUSAL ? j : 0;
@@ -586,7 +617,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          const bool in = 8 * u < lim;
+          const bool in = 8 * u < lim && dbg_row(dbb, bh, gk, g * (D / 2) + 8 * u, 8, kChkRowLoad);
           const uint4 kv = in ? __ldg(reinterpret_cast<const uint4*>(p.k + base) + u) : z;
           const uint4 vv = in ? __ldg(reinterpret_cast<const uint4*>(p.v + base) + u) : z;
           kw[4 * u] = kv.x, kw[4 * u + 1] = kv.y, kw[4 * u + 2] = kv.z, kw[4 * u + 3] = kv.w;
@@ -596,8 +627,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
 #pragma unroll
         for (int w = 0; w < 4 * kU; ++w) kw[w] = vw[w] = 0u;
       }
-      tmem_st_words(tmem_base + lane_bits + L::kKCol + g * (D / 4), kw);
-      tmem_st_words(tmem_base + lane_bits + L::kVCol + g * (D / 4), vw);
+      if (dbg_warp(dbg_tmem(dbb, tmem_base + lane_bits + L::kKCol + g * (D / 4), D / 4, warp,
+                            kChkRowTmem) &&
+                   dbg_tmem(dbb, tmem_base + lane_bits + L::kVCol + g * (D / 4), D / 4, warp,
+                            kChkRowTmem))) {
+        tmem_st_words(tmem_base + lane_bits + L::kKCol + g * (D / 4), kw);
+        tmem_st_words(tmem_base + lane_bits + L::kVCol + g * (D / 4), vw);
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(L::kKVTmem));
@@ -613,6 +649,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       if (!ok) break;
       tc_fence_after_sync();
       uint32_t s[32], dp[32];
+      if (!dbg_warp(dbg_tmem(dbb, tS, 32, warp, kChkSTmem) && dbg_tmem(dbb, tP, 32, warp, kChkSTmem))) {
+        ok = false;
+        break;
+      }
       tmem_ld_32x32b_x32(tS, s);
       tmem_ld_32x32b_x32(tP, dp);
       tmem_ld_wait();
@@ -664,7 +704,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
 #pragma unroll
       for (int c = 0; c < L::kChunks; ++c)
         store_chunk<F16>(tAcc + c * 64, stage + c * kChunkBytes, r, mul, map, c * 64, j * kTileRows,
-                         bh, wq, lane);
+                         bh, wq, lane, dbb);
       if (lane == 0) {
         tma_store_commit();
         tma_store_wait_all();
@@ -695,7 +735,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       for (int t = 0; t < 4; ++t) {
         const int c = lane + 32 * t;
         const int q = i * kTileRows + c;
-        const bool in = q < p.S;
+        const bool in = q < p.S && dbg_row(dbb, bh, q, 0, 0, kChkStat);
         st_shared_f32x2(stat + 8 * c, in ? p.lse[row0 + q] * kLog2e : 0.f,
                         in ? p.delta[row0 + q] : 0.f);
       }
@@ -704,10 +744,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
         mbar_arrive_expect_tx(bar(L::kFull + st), 2 * L::kTile);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_3d(sb + L::kQOff + st * L::kTile + c * kChunkBytes, &p.tm_q, bar(L::kFull + st),
-                      c * 64, i * kTileRows, bh, pol_q);
-          tma_load_3d(sb + L::kDoOff + st * L::kTile + c * kChunkBytes, &p.tm_do,
-                      bar(L::kFull + st), c * 64, i * kTileRows, bh, pol_q);
+          // a skipped copy leaves the stage's transaction count short: the
+          // consumer's bounded wait then ends the kernel
+          const uint32_t dq_dst = sb + L::kQOff + st * L::kTile + c * kChunkBytes;
+          const uint32_t do_dst = sb + L::kDoOff + st * L::kTile + c * kChunkBytes;
+          if (dbg_tma(dbb, dq_dst, kChunkBytes, c * 64, i * kTileRows, bh, false, kChkLoadA))
+            tma_load_3d(dq_dst, &p.tm_q, bar(L::kFull + st), c * 64, i * kTileRows, bh, pol_q);
+          if (dbg_tma(dbb, do_dst, kChunkBytes, c * 64, i * kTileRows, bh, false, kChkLoadB))
+            tma_load_3d(do_dst, &p.tm_do, bar(L::kFull + st), c * 64, i * kTileRows, bh, pol_q);
         }
       }
       issued = it + 1;
@@ -743,6 +787,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
     // buffer t & 1; A (K, V) from TMEM, 8 columns per K step of 16
     auto issue_sp = [&](int t) {
       const int b = t & 1, q = t & 3, st = (t >> 2) % L::kStages;
+      if (!dbg_smem(dbb, sb + L::kQOff + st * L::kTile, L::kTile, 1024, kChkMmaA) ||
+          !dbg_smem(dbb, sb + L::kDoOff + st * L::kTile, L::kTile, 1024, kChkMmaB))
+        return;  // S never completes: the elementwise warps' bounded wait ends the kernel
       const uint32_t bq = st * kTileUnits + q * kQuarterUnits;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {

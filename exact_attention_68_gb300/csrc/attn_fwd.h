@@ -32,6 +32,7 @@ struct FwdParams {
   float* lse;        // [B·H, S]
   int* status;       // device status word pair (error bits, first wait site)
   int B, H, S;
+  int d_cols;        // the tensors' head dimension (<= D, a multiple of 8)
   int n_qt;          // ceil(S / 128)
   int n_units;       // ceil(n_qt / 2): work units per (b, h)
   UnitSchedule sched;  // CTA index -> (b·H + h, unit level)

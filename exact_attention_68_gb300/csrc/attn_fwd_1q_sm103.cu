@@ -71,6 +71,9 @@ struct Layout1Q {
 enum : int { kSiteProdK = 0x3100, kSiteProdV = 0x3200, kSiteMmaQ = 0x3300, kSiteMmaK = 0x3400,
              kSiteMmaV = 0x3500, kSiteMmaP = 0x3600, kSiteSoftS = 0x3700, kSiteSoftPv = 0x3800,
              kSiteSoftO = 0x3900 };
+// debug-check sites (-DATTN_DEBUG)
+enum : int { kChkQLoad = 0x5101, kChkQTmem, kChkSTmem, kChkPTmem, kChkOTmem, kChkStage, kChkStore,
+             kChkLse, kChkLoadK, kChkLoadV, kChkMmaK, kChkMmaV, kChkMmaTmem };
 
 template <int D, int BN, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid_constant__ Fwd1QParams p) {
@@ -92,6 +95,8 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
   const uint32_t abort_addr = sb + kMiscOff + 4;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const DbgBounds dbb{p.status, sb, smem_u32(smem_raw) + static_cast<uint32_t>(L::kAlloc), p.S,
+                      p.d_cols, p.BH};
 
   // Q tile i of slice bh, in the order of the grid schedule (schedule.h):
   // heavy tiles by L2-sized groups of heads, then the light ones over all heads
@@ -148,11 +153,13 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int col = 64 * c + 8 * u;
-          const uint4 x = valid && col < p.d_cols ? __ldg(reinterpret_cast<const uint4*>(qr + col))
-                                                  : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 x = valid && col < p.d_cols && dbg_row(dbb, bh, grow, col, 8, kChkQLoad)
+                              ? __ldg(reinterpret_cast<const uint4*>(qr + col))
+                              : make_uint4(0u, 0u, 0u, 0u);
           w[4 * u] = x.x, w[4 * u + 1] = x.y, w[4 * u + 2] = x.z, w[4 * u + 3] = x.w;
         }
-        tmem_st_32x32b_x32(tmem_base + lane_bits + kQCol + 32 * c, w);
+        if (dbg_warp(dbg_tmem(dbb, tmem_base + lane_bits + kQCol + 32 * c, 32, warp, kChkQTmem)))
+          tmem_st_32x32b_x32(tmem_base + lane_bits + kQCol + 32 * c, w);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -171,6 +178,10 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
       tc_fence_after_sync();
       const uint32_t tS = tmem_base + lane_bits + BN * b;
       uint32_t s[BN / 32][32];
+      if (!dbg_warp(dbg_tmem(dbb, tS, BN, warp, kChkSTmem))) {
+        ok = false;
+        break;
+      }
 #pragma unroll
       for (int g = 0; g < BN / 32; ++g) tmem_ld_32x32b_x32(tS + 32 * g, s[g]);
       tmem_ld_wait();
@@ -225,8 +236,10 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       const bool any_moved = __any_sync(0xffffffffu, moved);  // every lane, no short-circuit
       if (!spec || any_moved) exps(neg_m);
+      if (dbg_warp(dbg_tmem(dbb, tS, BN / 2, warp, kChkPTmem))) {
 #pragma unroll
-      for (int g = 0; g < BN / 64; ++g) tmem_st_32x32b_x32(tS + 32 * g, pk[g]);
+        for (int g = 0; g < BN / 64; ++g) tmem_st_32x32b_x32(tS + 32 * g, pk[g]);
+      }
       const float2 ra = __fadd2_rn(__fadd2_rn(rs2[0], rs2[1]), __fadd2_rn(rs2[2], rs2[3]));
       const float rs0 = ra.x, rs1 = ra.y;
       const float rs = rs0 + rs1;
@@ -242,7 +255,8 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
           if (!ok) break;
           tc_fence_after_sync();
 #pragma unroll 1
-          for (int c = 0; c < kD / 32; ++c) {
+          for (int c = 0; c < kD / 32 && dbg_warp(dbg_tmem(dbb, tO + 32 * c, 32, warp, kChkOTmem));
+               ++c) {
             uint32_t o[32];
             tmem_ld_32x32b_x32(tO + 32 * c, o);
             tmem_ld_wait();
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
       const float inv_l = lq > 0.f ? 1.f / lq : 0.f;
       // 4 column blocks of 64 (128 bytes per row), 128 rows each (16 KB)
 #pragma unroll 1
-      for (int c = 0; c < kD / 32; ++c) {
+      for (int c = 0; c < kD / 32 && dbg_warp(dbg_tmem(dbb, tO + 32 * c, 32, warp, kChkOTmem)); ++c) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(tO + 32 * c, o);
         tmem_ld_wait();
@@ -280,20 +294,25 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
           for (int e = 0; e < 4; ++e)
             w[e] = pack_x2<F16>(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
                                 __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
-          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          if (dbg_smem(dbb, addr, 16, 16, kChkStage)) st_shared_v4(addr, w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      // this warp's 32 rows, if any of them is inside the tensor; a chunk
+      // wholly past the tensor's columns is not stored either
+      const int y0 = i * kQRows + warp * 32;
+      if (lane == 0 && y0 < p.S) {
 #pragma unroll
-        for (int c = 0; c < kD / 64; ++c)
-          if (64 * c < p.d_cols)  // a chunk wholly past the tensor's columns is not stored
-            tma_store_3d(&p.tm_o, sb + kKOff + c * (kQRows * 128) + warp * 32 * 128, c * 64,
-                         i * kQRows + warp * 32, bh);
+        for (int c = 0; c < kD / 64; ++c) {
+          const uint32_t src = sb + kKOff + c * (kQRows * 128) + warp * 32 * 128;
+          if (64 * c < p.d_cols && dbg_tma(dbb, src, 32 * 128, c * 64, y0, bh, true, kChkStore))
+            tma_store_3d(&p.tm_o, src, c * 64, y0, bh);
+        }
         tma_store_commit();
       }
-      if (valid) p.lse[(int64_t)bh * p.S + grow] = (m + __log2f(l)) * kLn2;
+      if (valid && dbg_row(dbb, bh, grow, 0, 0, kChkLse))
+        p.lse[(int64_t)bh * p.S + grow] = (m + __log2f(l)) * kLn2;
       if (lane == 0) tma_store_wait_all();
     }
     tc_fence_before_sync();
@@ -312,18 +331,24 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
         if (!ok) break;
         mbar_arrive_expect_tx(bar(kKFull + ks), kTile);
 #pragma unroll
-        for (int c = 0; c < kD / 64; ++c)
-          tma_load_3d(sb + kKOff + ks * kTile + c * kChunkBytes, &p.tm_k, bar(kKFull + ks), c * 64,
-                      j * kKvRows, bh, pol);
+        for (int c = 0; c < kD / 64; ++c) {
+          // a skipped copy leaves the stage's transaction count short: the
+          // consumer's bounded wait then ends the kernel
+          const uint32_t dst = sb + kKOff + ks * kTile + c * kChunkBytes;
+          if (dbg_tma(dbb, dst, kChunkBytes, c * 64, j * kKvRows, bh, false, kChkLoadK))
+            tma_load_3d(dst, &p.tm_k, bar(kKFull + ks), c * 64, j * kKvRows, bh, pol);
+        }
         k_issued = j + 1;
         const int vs = j % kVStages;
         ok = wait_bounded(bar(kVEmpty + vs), ((j / kVStages) & 1) ^ 1, ctl, kSiteProdV | (j & 0xff));
         if (!ok) break;
         mbar_arrive_expect_tx(bar(kVFull + vs), kTile);
 #pragma unroll
-        for (int c = 0; c < kD / 64; ++c)
-          tma_load_3d(sb + kVOff + vs * kTile + c * kChunkBytes, &p.tm_v, bar(kVFull + vs), c * 64,
-                      j * kKvRows, bh, pol);
+        for (int c = 0; c < kD / 64; ++c) {
+          const uint32_t dst = sb + kVOff + vs * kTile + c * kChunkBytes;
+          if (dbg_tma(dbb, dst, kChunkBytes, c * 64, j * kKvRows, bh, false, kChkLoadV))
+            tma_load_3d(dst, &p.tm_v, bar(kVFull + vs), c * 64, j * kKvRows, bh, pol);
+        }
         v_issued = j + 1;
       }
       if (ok) {
@@ -352,6 +377,10 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
     };
     // S(j) into buffer j & 1: Q (TMEM, 8 columns per K step) · K_jᵀ (K-major)
     auto issue_s = [&](int j) {
+      if (!dbg_smem(dbb, sb + kKOff + (j % kKStages) * kTile, kTile, 1024, kChkMmaK) ||
+          !dbg_tmem_cols(dbb, tmem_base + BN * (j & 1), BN, kChkMmaTmem) ||
+          !dbg_tmem_cols(dbb, tmem_base + kQCol, kD / 2, kChkMmaTmem))
+        return;  // no commit: the softmax's bounded wait ends the kernel
       const uint64_t db = dk + (j % kKStages) * kTileUnits;
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
@@ -376,7 +405,8 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
       if (ok) ok = wait_warp(bar(kVFull + j % kVStages), (j / kVStages) & 1, kSiteMmaV | (j & 0xff));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader) {
+      if (leader && dbg_smem(dbb, sb + kVOff + (j % kVStages) * kTile, kTile, 1024, kChkMmaV) &&
+          dbg_tmem_cols(dbb, tmem_base + kOCol, kD, kChkMmaTmem)) {
         const uint64_t db = dv + (j % kVStages) * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < kKvRows / 16; ++kk)  // O += P_b · V_j, 16 keys per step

@@ -86,6 +86,9 @@ enum : int {
   kSiteProducerK = 0x100, kSiteProducerV = 0x200, kSiteMmaQ = 0x300, kSiteMmaK = 0x400,
   kSiteMmaV = 0x500, kSiteMmaP = 0x600, kSiteSoftS = 0x700, kSiteSoftO = 0x800
 };
+// debug-check sites (-DATTN_DEBUG)
+enum : int { kChkSTmem = 0x5001, kChkOTmem, kChkStage, kChkStore, kChkLse, kChkLoadQ, kChkLoadK,
+             kChkLoadV, kChkMmaQ, kChkMmaK, kChkMmaV, kChkMmaTmem };
 
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -99,6 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const DbgBounds dbb{p.status, sb, smem_u32(smem_raw) + static_cast<uint32_t>(L::kAlloc), p.S,
+                      p.d_cols, p.B * p.H};
 
   // ---- work unit: (b·H + h, pair of Q tiles), from the grid schedule
   int bh, u;
@@ -171,6 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // S_j arrives in two 64-column halves: the second half's TMEM load is in
       // flight while the first half is processed.
       uint32_t sr[4][32];
+      if (!dbg_warp(dbg_tmem(dbb, tS, 128, warp, kChkSTmem))) {  // S_j, then P_j over it
+        ok = false;
+        break;
+      }
       tmem_ld_32x32b_x32(tS + 0, sr[0]);
       tmem_ld_32x32b_x32(tS + 32, sr[1]);
       tmem_ld_wait();
@@ -270,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       lq = lq * alpha + (rs + (pmax_q - pmax));
       // correction: rescale this row of O when its reference max moved.  PV_{j-1}
       // has completed: S_j was committed after it.
-      if (moved_before) {
+      if (moved_before && dbg_warp(dbg_tmem(dbb, tO, D, warp, kChkOTmem))) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -293,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ok = wait_bounded(bar(L::kOFull + t), 0, ctl, kSiteSoftO | t);
         ok = __all_sync(0xffffffffu, ok);
       }
+      if (ok) ok = dbg_warp(dbg_tmem(dbb, tO, D, warp, kChkOTmem));
       if (ok) {
         tc_fence_after_sync();
         const float inv_l = lq > 0.f ? 1.f / lq : 0.f;
@@ -316,19 +326,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             for (int e = 0; e < 4; ++e)
               w[e] = pack_x2<F16>(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
                                  __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
-            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+            if (dbg_smem(dbb, addr, 16, 16, kChkStage)) st_shared_v4(addr, w[0], w[1], w[2], w[3]);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        const int y0 = qt * kBlockM + wq * 32;  // stored if any of its 32 rows is inside
+        if (lane == 0 && y0 < p.S) {
 #pragma unroll
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_store_3d(&p.tm_o, stage + c * L::kChunkBytes + wq * 32 * 128, c * 64,
-                         qt * kBlockM + wq * 32, bh);
+          for (int c = 0; c < L::kChunks; ++c) {
+            const uint32_t src = stage + c * L::kChunkBytes + wq * 32 * 128;
+            if (dbg_tma(dbb, src, 32 * 128, c * 64, y0, bh, true, kChkStore))
+              tma_store_3d(&p.tm_o, src, c * 64, y0, bh);
+          }
           tma_store_commit();
         }
-        if (grow < p.S) p.lse[(int64_t)bh * p.S + grow] = (m + __log2f(l)) * kLn2;
+        if (grow < p.S && dbg_row(dbb, bh, grow, 0, 0, kChkLse))
+          p.lse[(int64_t)bh * p.S + grow] = (m + __log2f(l)) * kLn2;
         if (lane == 0) tma_store_wait_all();
       }
     }
@@ -349,9 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if ((t == 0 ? n0 : n1) == 0) continue;
         mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sb + L::kQOff + t * L::kTileBytes + c * L::kChunkBytes, &p.tm_q,
-                      bar(L::kQFull + t), c * 64, (t == 0 ? qt0 : qt1) * kBlockM, bh, pol_q);
+        for (int c = 0; c < L::kChunks; ++c) {
+          // a skipped copy leaves the stage's transaction count short: the
+          // consumer's bounded wait then ends the kernel
+          const uint32_t dst = sb + L::kQOff + t * L::kTileBytes + c * L::kChunkBytes;
+          const int y = (t == 0 ? qt0 : qt1) * kBlockM;
+          if (dbg_tma(dbb, dst, L::kChunkBytes, c * 64, y, bh, false, kChkLoadQ))
+            tma_load_3d(dst, &p.tm_q, bar(L::kQFull + t), c * 64, y, bh, pol_q);
+        }
       }
       int k_issued = 0, v_issued = 0;  // K / V tiles whose loads were issued
       bool ok = true;
@@ -361,18 +380,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!ok) break;
         mbar_arrive_expect_tx(bar(L::kKFull + ks), L::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sb + L::kKOff + ks * L::kTileBytes + c * L::kChunkBytes, &p.tm_k,
-                      bar(L::kKFull + ks), c * 64, j * kBlockN, bh, pol_kv);
+        for (int c = 0; c < L::kChunks; ++c) {
+          const uint32_t dst = sb + L::kKOff + ks * L::kTileBytes + c * L::kChunkBytes;
+          if (dbg_tma(dbb, dst, L::kChunkBytes, c * 64, j * kBlockN, bh, false, kChkLoadK))
+            tma_load_3d(dst, &p.tm_k, bar(L::kKFull + ks), c * 64, j * kBlockN, bh, pol_kv);
+        }
         k_issued = j + 1;
         const int vs = j % L::kVStages;
         ok = wait_bounded(bar(L::kVEmpty + vs), ((j / L::kVStages) & 1) ^ 1, ctl, kSiteProducerV | j);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(L::kVFull + vs), L::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sb + L::kVOff + vs * L::kTileBytes + c * L::kChunkBytes, &p.tm_v,
-                      bar(L::kVFull + vs), c * 64, j * kBlockN, bh, pol_kv);
+        for (int c = 0; c < L::kChunks; ++c) {
+          const uint32_t dst = sb + L::kVOff + vs * L::kTileBytes + c * L::kChunkBytes;
+          if (dbg_tma(dbb, dst, L::kChunkBytes, c * 64, j * kBlockN, bh, false, kChkLoadV))
+            tma_load_3d(dst, &p.tm_v, bar(L::kVFull + vs), c * 64, j * kBlockN, bh, pol_kv);
+        }
         v_issued = j + 1;
       }
       if (ok) {
@@ -414,6 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // S_t = Q_t · K_stageᵀ: D/16 MMAs of K = 16 (32 bytes within a 128-byte
       // swizzle row; the next 64 columns are the next 16 KB block).
       auto issue_s = [&](int t, int ks) {
+        if (!dbg_smem(dbb, sb + L::kQOff + t * L::kTileBytes, L::kTileBytes, 1024, kChkMmaQ) ||
+            !dbg_smem(dbb, sb + L::kKOff + ks * L::kTileBytes, L::kTileBytes, 1024, kChkMmaK) ||
+            !dbg_tmem_cols(dbb, tmem_base + t * 128, 128, kChkMmaTmem))
+          return;  // S_t never completes: the softmax's bounded wait ends the kernel
         const uint64_t da = dq + t * kTileUnits;
         const uint64_t db = dk + ks * kTileUnits;
 #pragma unroll
@@ -424,6 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       };
       // O_t += P_t · V_stage: 8 MMAs of K = 16 key rows (2 KB of V each).
       auto issue_pv = [&](int t, int vs, bool accumulate) {
+        if (!dbg_smem(dbb, sb + L::kVOff + vs * L::kTileBytes, L::kTileBytes, 1024, kChkMmaV) ||
+            !dbg_tmem_cols(dbb, tmem_base + 256 + t * D, D, kChkMmaTmem))
+          return;
         const uint64_t db = dv + vs * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)

@@ -46,6 +46,12 @@ inline cudaError_t current_device_bound(int* dev) {
 // most 256): the smallest of 64, 128, 256 that holds D.
 inline int kernel_head_dim(int64_t D) { return D <= 64 ? 64 : D <= 128 ? 128 : 256; }
 
+// The status a non-zero device status word reports: its bits are 1 (a wait
+// ran out) and 2 (an index check of a debug build failed).
+inline attn_status_t status_of_words(int bits) {
+  return (bits & 2) ? ATTN_ERR_DEVICE_CHECK : ATTN_ERR_TIMEOUT;
+}
+
 // True if the byte ranges [a, a+na) and [b, b+nb) intersect.
 inline bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);

@@ -96,5 +96,5 @@ extern "C" attn_status_t attn_fwd_noalloc(const void* q, const void* k, const vo
   if (cudaMemcpyAsync(words, scratch, sizeof(words), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  return words[0] != 0 ? ATTN_ERR_TIMEOUT : ATTN_OK;
+  return words[0] != 0 ? ea::status_of_words(words[0]) : ATTN_OK;
 }

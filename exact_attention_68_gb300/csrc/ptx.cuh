@@ -101,7 +101,7 @@ struct WaitCtl {
 constexpr uint32_t kSuspendHintNs = 200000;
 
 // Device status bits (combined with atomicOr in the global status word).
-enum : int { kStatusTimeout = 1 };
+enum : int { kStatusTimeout = 1, kStatusBounds = 2 };
 
 static __device__ __noinline__ void raise_abort(const WaitCtl& c, int where) {
   st_volatile_shared(c.abort_flag, 1);
@@ -126,6 +126,95 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
       return false;
     }
   }
+}
+
+// ---------------------------------------------------------------- debug checks
+// Built with -DATTN_DEBUG, the kernels check the index arithmetic of each
+// memory access before making it: TMA coordinates (16-byte column alignment,
+// boxes that start inside the tensor), shared- and tensor-memory addresses
+// against the CTA's allocation, and the row and column of every plain global
+// load or store.  A failed check sets kStatusBounds and the site in the
+// status words, and the access is skipped, so a bad index never reaches
+// memory.  Release builds compile every check to `true`.
+#ifdef ATTN_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+struct DbgBounds {
+  int* status;        // status words (may be null)
+  uint32_t smem_lo;   // the CTA's dynamic shared memory, [smem_lo, smem_hi)
+  uint32_t smem_hi;
+  int rows;           // rows of one (b, h) slice: S
+  int cols;           // columns of the 16-bit tensors: the head dimension
+  int slices;         // B·H
+};
+
+static __device__ __noinline__ void dbg_fail(int* status, int site) {
+  if (status != nullptr) {
+    atomicOr(status, kStatusBounds);
+    atomicCAS(status + 1, 0, site);
+  }
+}
+
+__device__ __forceinline__ bool dbg(bool ok, const DbgBounds& d, int site) {
+  if (!kDebugChecks || ok) return true;
+  dbg_fail(d.status, site);
+  return false;
+}
+
+// `bytes` of shared memory at `addr`, aligned to `align` (a power of two).
+__device__ __forceinline__ bool dbg_smem(const DbgBounds& d, uint32_t addr, uint32_t bytes,
+                                         uint32_t align, int site) {
+  if (!kDebugChecks) return true;
+  return dbg(addr >= d.smem_lo && addr + bytes <= d.smem_hi && (addr & (align - 1)) == 0, d, site);
+}
+
+// A tiled TMA copy of a 128-byte-swizzled box into (or out of) `bytes` of
+// shared memory at `saddr`, at tensor coordinates (x, y, z): x a multiple of 8
+// 16-bit values (16 bytes) and not negative, the box's first row and slice
+// inside the tensor (a load may run past the end and reads zeros there; a
+// store must start inside the tensor's columns too).
+__device__ __forceinline__ bool dbg_tma(const DbgBounds& d, uint32_t saddr, uint32_t bytes, int x,
+                                        int y, int z, bool store, int site) {
+  if (!kDebugChecks) return true;
+  const bool coords = x >= 0 && (x & 7) == 0 && y >= 0 && y < d.rows && z >= 0 && z < d.slices &&
+                      (!store || x < d.cols);
+  return dbg(coords && saddr >= d.smem_lo && saddr + bytes <= d.smem_hi && (saddr & 1023) == 0, d,
+             site);
+}
+
+// `ncols` tensor-memory columns from the address `taddr` (lane << 16 | column)
+// of a 512-column allocation, in the lane quarter of warp `warp`.
+__device__ __forceinline__ bool dbg_tmem(const DbgBounds& d, uint32_t taddr, uint32_t ncols,
+                                         int warp, int site) {
+  if (!kDebugChecks) return true;
+  const uint32_t col = taddr & 0xffffu, lane = taddr >> 16;
+  return dbg(col + ncols <= 512u && lane == 32u * static_cast<uint32_t>(warp & 3), d, site);
+}
+
+// The same for an MMA operand or accumulator (any lane quarter).
+__device__ __forceinline__ bool dbg_tmem_cols(const DbgBounds& d, uint32_t taddr, uint32_t ncols,
+                                              int site) {
+  if (!kDebugChecks) return true;
+  return dbg((taddr & 0xffffu) + ncols <= 512u && (taddr >> 16) == 0u, d, site);
+}
+
+// A check whose outcome a whole warp acts on (it guards a warp-collective
+// instruction): every lane gets the warp's verdict.  Call with the full warp.
+__device__ __forceinline__ bool dbg_warp(bool ok) {
+  if (!kDebugChecks) return true;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// A plain global access of `n` 16-bit values at column `col` of row `row` of
+// slice `bh`, or (n = 0) of one per-row fp32 value.
+__device__ __forceinline__ bool dbg_row(const DbgBounds& d, int bh, int row, int col, int n,
+                                        int site) {
+  if (!kDebugChecks) return true;
+  return dbg(bh >= 0 && bh < d.slices && row >= 0 && row < d.rows && col >= 0 && col + n <= d.cols,
+             d, site);
 }
 
 // Wait used only while tearing down after an abort: ignores the abort flag,

@@ -60,7 +60,10 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2,  /* head_dim not a multiple of 8 or above 256 (128 for the backward), or no sm_103a device */
   ATTN_ERR_MISALIGNED = 3,   /* a pointer not 16-byte aligned */
   ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, copy, tensor-map encode) */
-  ATTN_ERR_TIMEOUT = 5       /* a bounded in-kernel wait ran out (reported by attn_device_status) */
+  ATTN_ERR_TIMEOUT = 5,      /* a bounded in-kernel wait ran out (reported by attn_device_status) */
+  ATTN_ERR_DEVICE_CHECK = 6  /* a debug build's in-kernel index check failed; the access was
+                                skipped (reported by attn_device_status; release builds have
+                                no such checks) */
 } attn_status_t;
 
 /* The 16-bit type of q, k, v, out (and dout, dq, dk, dv) for the _ex entry points. */
@@ -134,8 +137,10 @@ ATTN_API attn_status_t attn_fwd_bounded(const void* q, const void* k, const void
 
 /*
  * attn_device_status — synchronise `stream`, then read and clear the status
- * word of the current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel on
- * this device recorded a timeout since the last read) or ATTN_ERR_CUDA.
+ * word of the current device.  Returns ATTN_OK, ATTN_ERR_DEVICE_CHECK (a kernel
+ * of a debug build recorded a failed index check since the last read),
+ * ATTN_ERR_TIMEOUT (a kernel on this device recorded a timeout since the last
+ * read) or ATTN_ERR_CUDA.
  */
 ATTN_API attn_status_t attn_device_status(cudaStream_t stream);
 
@@ -154,7 +159,8 @@ ATTN_API attn_status_t attn_device_status(cudaStream_t stream);
  *
  * Arguments, layout, ownership and argument errors are those of attn_fwd.
  * check_status: 0 = return once enqueued; 1 = also synchronise `stream` and
- * return ATTN_ERR_TIMEOUT if this call's kernel recorded a wait that ran out.
+ * return ATTN_ERR_TIMEOUT if this call's kernel recorded a wait that ran out
+ * (ATTN_ERR_DEVICE_CHECK for a failed index check of a debug build).
  * The scratch this kernel needs (two status words, 8 bytes) does not grow with
  * B, H, S or D; a need above ATTN_NOALLOC_SCRATCH_BYTES is rejected with
  * ATTN_ERR_INVALID_ARG before anything is enqueued.

@@ -37,9 +37,21 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
-        assert lib.attn_status_string(code)
+    for code in range(7):
+        assert lib.attn_status_string(code) != b"unknown status"
     assert lib.attn_status_string(0) == b"ok"
+    assert b"debug" in lib.attn_status_string(binding.ATTN_ERR_DEVICE_CHECK)
+
+
+def test_debug_build_compiles_and_exports_the_abi():
+    """The -DATTN_DEBUG variant (in-kernel index checks) builds for sm_103a
+    and exports the same C ABI; its kernels run in the GPU tests."""
+    from exact_attention_68_gb300.build import build_debug_library
+    path = build_debug_library()
+    dbg = binding.load_library(path)
+    for name in binding.EXPORTED_SYMBOLS:
+        assert hasattr(dbg, name), name
+    assert dbg.attn_abi_version() == 1
 
 
 # Fake, never dereferenced device addresses: validation runs before any CUDA call.
