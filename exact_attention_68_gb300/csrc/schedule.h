@@ -95,10 +95,25 @@ inline int staged_chunk_count(int64_t BH, int64_t in_bytes_per_slice, int64_t ta
   return static_cast<int>(n);
 }
 
-// Slices [*first, *first + *count) of chunk c of n: the slices are spread
-// evenly, the first BH % n chunks taking one more.
+// Slices [*first, *first + *count) of chunk c of n (n <= BH).  The last
+// chunk takes half an even share (at least one slice): its kernel and its
+// download are the part of the call that no upload hides.  The other chunks
+// share the rest evenly, the first ones taking one more.
 inline void staged_chunk_range(int64_t BH, int n, int c, int64_t* first, int64_t* count) {
-  const int64_t base = BH / n, rem = BH % n;
+  if (n <= 1) {
+    *first = 0;
+    *count = BH;
+    return;
+  }
+  int64_t last = BH / n / 2;
+  if (last < 1) last = 1;
+  const int64_t rest = BH - last;  // >= n - 1
+  if (c == n - 1) {
+    *first = rest;
+    *count = last;
+    return;
+  }
+  const int64_t base = rest / (n - 1), rem = rest % (n - 1);
   *count = base + (c < rem ? 1 : 0);
   *first = c * base + (c < rem ? c : rem);
 }

@@ -128,7 +128,12 @@ def test_staged_chunk_plan_covers_every_slice_once(shim, BH, per_slice_mb):
     assert first[0] == 0 and all(x >= 1 for x in count)
     assert all(first[c] + count[c] == first[c + 1] for c in range(n - 1))
     assert first[-1] + count[-1] == BH
-    assert max(count) - min(count) <= 1
+    # all but the last chunk even; the last one half an even share (>= 1)
+    if n > 1:
+        assert max(count[:-1]) - min(count[:-1]) <= 1
+        assert count[-1] == max(1, BH // n // 2) and count[-1] <= min(count[:-1])
+    else:
+        assert count == [BH]
     # as many chunks as the inputs need at about `target` bytes each, capped
     want = -(-BH * (per_slice_mb << 20) // target)
     assert n == max(1, min(want, BH, max_chunks))
