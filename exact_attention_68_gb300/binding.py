@@ -144,10 +144,12 @@ def attn_fwd_bounded(q, k, v, scale=None, causal=True, out=None, lse=None, strea
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    if out.dtype != q.dtype or out.shape != q.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor shaped like q, of its dtype")
-    if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor")
+    if (out.dtype != q.dtype or out.shape != q.shape or not out.is_contiguous()
+            or out.device != q.device):
+        raise ValueError("out must be a contiguous tensor shaped like q, of its dtype and device")
+    if (lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous()
+            or lse.device != q.device):
+        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor on q's device")
     lib = load_library()
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
             B, H, S, D, float(scale), 1 if causal else 0)
@@ -171,8 +173,21 @@ def attn_fwd_staged(q_h, k_h, v_h, out_h, lse_h, q_d, k_d, v_d, out_d, lse_d, sc
     _check_qkv(q_d, k_d, v_d)
     B, H, S, D = q_d.shape
     for name, t in (("q_h", q_h), ("k_h", k_h), ("v_h", v_h), ("out_h", out_h), ("lse_h", lse_h)):
-        if t.is_cuda or not t.is_contiguous():
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous host tensor")
+    # the library copies whole [B, H, S, D] bf16 (and [B, H, S] fp32) buffers
+    # between these tensors: every one must have exactly that size and type
+    for name, t in (("q_h", q_h), ("k_h", k_h), ("v_h", v_h), ("out_h", out_h)):
+        if t.dtype != torch.bfloat16 or t.shape != q_d.shape:
+            raise ValueError(f"{name} must be a bf16 tensor shaped like q_d")
+    if lse_h.dtype != torch.float32 or lse_h.shape != (B, H, S):
+        raise ValueError("lse_h must be an fp32 [B, H, S] tensor")
+    if (not isinstance(out_d, torch.Tensor) or out_d.dtype != torch.bfloat16
+            or out_d.shape != q_d.shape or not out_d.is_contiguous() or out_d.device != q_d.device):
+        raise ValueError("out_d must be a contiguous bf16 tensor shaped like q_d, on its device")
+    if (not isinstance(lse_d, torch.Tensor) or lse_d.dtype != torch.float32
+            or lse_d.shape != (B, H, S) or not lse_d.is_contiguous() or lse_d.device != q_d.device):
+        raise ValueError("lse_d must be a contiguous fp32 [B, H, S] tensor on q_d's device")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     lib = load_library()
@@ -197,10 +212,12 @@ def attn_fwd_noalloc(q, k, v, out, lse, scale=None, causal=True, check_status=Tr
     B, H, S, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    if out.dtype != torch.bfloat16 or out.shape != q.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
-    if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor")
+    if (out.dtype != torch.bfloat16 or out.shape != q.shape or not out.is_contiguous()
+            or out.device != q.device):
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q, on its device")
+    if (lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous()
+            or lse.device != q.device):
+        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor on q's device")
     lib = load_library()
     with torch.cuda.device(q.device):
         rc = lib.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
@@ -237,10 +254,12 @@ def attn_bwd_bounded(q, k, v, out, lse, dout, scale=None, causal=True, dq=None, 
     dv = torch.empty_like(q) if dv is None else dv
     delta = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if delta is None else delta
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        if t.dtype != q.dtype or t.shape != q.shape or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous tensor shaped like q, of its dtype")
-    if delta.dtype != torch.float32 or delta.shape != (B, H, S) or not delta.is_contiguous():
-        raise ValueError("delta must be a contiguous fp32 [B, H, S] tensor")
+        if (t.dtype != q.dtype or t.shape != q.shape or not t.is_contiguous()
+                or t.device != q.device):
+            raise ValueError(f"{name} must be a contiguous tensor shaped like q, of its dtype and device")
+    if (delta.dtype != torch.float32 or delta.shape != (B, H, S) or not delta.is_contiguous()
+            or delta.device != q.device):
+        raise ValueError("delta must be a contiguous fp32 [B, H, S] tensor on q's device")
     lib = load_library()
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
             dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(),

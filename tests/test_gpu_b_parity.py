@@ -198,6 +198,43 @@ def test_binding_rejects_wrong_dtype_and_layout(cuda_device):
         binding.attn_fwd(q, k, v, scale=-1.0)
 
 
+def test_binding_rejects_outputs_of_the_wrong_size_type_or_device(cuda_device):
+    """Every buffer the library writes or copies must be exactly the size,
+    type and side (host or device) the call implies: checked in the binding
+    before anything is enqueued."""
+    shape = (1, 2, 128, 64)
+    q, k, v = (x.to("cuda:0") for x in make_qkv(shape))
+    out, lse = binding.attn_fwd(q, k, v)
+    with pytest.raises(ValueError):
+        binding.attn_fwd(q, k, v, out=torch.empty(shape, dtype=torch.bfloat16))  # host out
+    with pytest.raises(ValueError):
+        binding.attn_fwd(q, k, v, lse=torch.empty(shape[:3]))                     # host lse
+    dout = torch.ones_like(q)
+    with pytest.raises(ValueError):
+        binding.attn_bwd(q, k, v, out, lse, dout, dq=torch.empty(shape, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        binding.attn_bwd(q, k, v, out, lse, dout, delta=torch.empty(shape[:3]))
+    with pytest.raises(ValueError):
+        binding.attn_fwd_noalloc(q, k, v, torch.empty(shape, dtype=torch.bfloat16), lse)
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    hout = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(shape[:3]).pin_memory()
+    dq_, dk_, dv_ = (torch.empty_like(q) for _ in range(3))
+    dout_, dlse_ = torch.empty_like(q), torch.empty_like(lse)
+    small = torch.empty((1, 1, 128, 64), dtype=torch.bfloat16).pin_memory()
+    for bad in ({"q_h": small}, {"out_h": small}, {"lse_h": torch.empty((1, 2, 64))},
+                {"q_h": hq.float()}, {"out_d": dout_[:, :1]}, {"lse_d": dlse_.cpu()}):
+        kw = dict(q_h=hq, k_h=hk, v_h=hv, out_h=hout, lse_h=hlse, q_d=dq_, k_d=dk_, v_d=dv_,
+                  out_d=dout_, lse_d=dlse_)
+        kw.update(bad)
+        with pytest.raises(ValueError):
+            binding.attn_fwd_staged(**kw)
+    # the valid call still works and matches the device path
+    binding.attn_fwd_staged(hq, hk, hv, hout, hlse, dq_, dk_, dv_, dout_, dlse_)
+    torch.cuda.synchronize()
+    assert torch.equal(hout, out.cpu()) and torch.equal(hlse, lse.cpu())
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_long_context_131072(cuda_device, D):
     """The longest context here: S = 131072 (1024 Q tiles, 512 units of the
