@@ -308,6 +308,20 @@ def side_workloads(device, stream):
     ms = time_steps(lambda: binding.attn_fwd(q, k, v, scale, w.causal, out, lse), 20, stream) / 20
     res[WORKLOAD + "_fp16"] = {"about": w.about + ", fp16 inputs", "ms": ms,
                                "tflops": counted_flops(w.B, w.H, w.S, w.D, w.causal) / (ms * 1e-3) / 1e12}
+    # other head dimensions at the long-context shape (the same 16384-key rows):
+    # 256 has its own kernel width, 96 and 192 run on the next width up
+    for D, H in ((256, 16), (96, 32), (192, 16)):
+        gen = torch.Generator(device=device).manual_seed(D)
+        q, k, v = (torch.randn((1, H, 16384, D), generator=gen, device=device).to(torch.bfloat16)
+                   for _ in range(3))
+        out, lse = torch.empty_like(q), torch.empty(1, H, 16384, device=device)
+        scale = default_scale(D)
+        for _ in range(3):
+            binding.attn_fwd(q, k, v, scale, True, out, lse)
+        ms = time_steps(lambda: binding.attn_fwd(q, k, v, scale, True, out, lse), 10, stream) / 10
+        res[f"d{D}"] = {"about": f"causal B=1 H={H} S=16384 D={D}, N(0,1)", "ms": ms,
+                        "tflops": counted_flops(1, H, 16384, D, True) / (ms * 1e-3) / 1e12}
+        del q, k, v, out, lse
     return res
 
 
