@@ -32,6 +32,8 @@ constexpr uint64_t kWaitTimeoutNs = ATTN_DEFAULT_WAIT_TIMEOUT_NS;  // the bound 
 // Scratch the forward kernel needs: its two status words.  The need does not
 // grow with B, H, S or D.
 constexpr size_t kScratchNeedBytes = 2 * sizeof(int);
+static_assert(kScratchNeedBytes <= ATTN_NOALLOC_SCRATCH_BYTES,
+              "the kernel's scratch must fit the static array (a build-time limit)");
 
 static __device__ __align__(256) int g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES / sizeof(int)];
 
@@ -57,14 +59,16 @@ attn_status_t noalloc_setup(int** scratch) {
   NoAllocDevice& d = g_dev[dev];
   if (!d.ready) {
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    cudaError_t ae = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (ae == cudaSuccess) ae = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (ae != cudaSuccess) return ea::cuda_failure(static_cast<int>(ae));
     d.supported = (major == 10 && minor == 3);
     if (d.supported) {
       void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
-        return ATTN_ERR_CUDA;  // not marked ready: the next call tries again
+      const cudaError_t se = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      // not marked ready on failure: the next call tries again
+      if (se != cudaSuccess) return ea::cuda_failure(static_cast<int>(se));
+      if (ptr == nullptr) return ea::cuda_failure(static_cast<int>(cudaErrorInvalidSymbol));
       d.scratch = static_cast<int*>(ptr);
     }
     d.ready = true;
@@ -83,18 +87,26 @@ extern "C" attn_status_t attn_fwd_noalloc(const void* q, const void* k, const vo
   attn_status_t s = ea::validate_args(q, k, v, out, lse, B, H, S, D, scale, causal);
   if (s != ATTN_OK) return s;
   if (check_status != 0 && check_status != 1) return ATTN_ERR_INVALID_ARG;
-  if (kScratchNeedBytes > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_INVALID_ARG;
   int* scratch = nullptr;
   s = noalloc_setup(&scratch);
   if (s != ATTN_OK) return s;
+  if (check_status) {
+    // check_status synchronises the stream, which a stream being captured
+    // into a graph does not allow: refuse before anything is enqueued
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const cudaError_t ce = cudaStreamIsCapturing(stream, &cap);
+    if (ce != cudaSuccess) return ea::cuda_failure(static_cast<int>(ce));
+    if (cap != cudaStreamCaptureStatusNone) return ATTN_ERR_INVALID_ARG;
+  }
   // The array keeps the previous call's words: clear them for this call.
-  if (cudaMemsetAsync(scratch, 0, kScratchNeedBytes, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(scratch, 0, kScratchNeedBytes, stream);
+  if (e != cudaSuccess) return ea::cuda_failure(static_cast<int>(e));
   s = ea::launch_with_status(q, k, v, out, lse, B, H, S, D, scale, causal, /*f16=*/false,
                              kWaitTimeoutNs, scratch, stream);
   if (s != ATTN_OK || !check_status) return s;
   int words[2] = {0, 0};
-  if (cudaMemcpyAsync(words, scratch, sizeof(words), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-      cudaStreamSynchronize(stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  e = cudaMemcpyAsync(words, scratch, sizeof(words), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return ea::cuda_failure(static_cast<int>(e));
   return words[0] != 0 ? ea::status_of_words(words[0]) : ATTN_OK;
 }

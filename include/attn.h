@@ -25,11 +25,15 @@
  * row-major bf16 tensors of shape [B, H, S, D]; lse is contiguous fp32
  * [B, H, S].  Query and key lengths are equal (S).
  *
- * Ownership: the caller owns every buffer.  Apart from one small device
- * status word per device (allocated on the first call on that device and kept
- * until process exit) the library allocates nothing, keeps no reference to any
- * buffer after a call returns, and never synchronises the stream inside
- * attn_fwd.  Entry points are thread-safe and reentrant.
+ * Ownership: the caller owns every buffer.  The library keeps, per device and
+ * until process exit: one pair of device status words (cudaMalloc'd on the
+ * first call on that device), three streams and a few events for
+ * attn_fwd_staged (created on its first call on that device), and the static
+ * ATTN_NOALLOC_SCRATCH_BYTES array of attn_fwd_noalloc (part of the loaded
+ * module on every GPU that loads the library).  Beyond that it allocates
+ * nothing, keeps no reference to any buffer after a call returns, and never
+ * synchronises the stream inside attn_fwd.  Entry points are thread-safe and
+ * reentrant.
  *
  * Error behaviour: argument errors are reported before anything is launched
  * and nothing is written.  A failed launch returns ATTN_ERR_CUDA.  Every wait
@@ -158,12 +162,18 @@ ATTN_API attn_status_t attn_device_status(cudaStream_t stream);
  * cudaMalloc, cudaFree or other allocating routine.
  *
  * Arguments, layout, ownership and argument errors are those of attn_fwd.
- * check_status: 0 = return once enqueued; 1 = also synchronise `stream` and
- * return ATTN_ERR_TIMEOUT if this call's kernel recorded a wait that ran out
- * (ATTN_ERR_DEVICE_CHECK for a failed index check of a debug build).
+ * check_status: 1 = also synchronise `stream` and return ATTN_ERR_TIMEOUT if
+ * this call's kernel recorded a wait that ran out (ATTN_ERR_DEVICE_CHECK for a
+ * failed index check of a debug build).  A stream that is being captured into
+ * a graph cannot be synchronised, so check_status = 1 on such a stream is
+ * rejected with ATTN_ERR_INVALID_ARG before anything is enqueued.
+ * 0 = return once enqueued, giving up that report: no entry point reads the
+ * static array's status words (attn_device_status reads attn_fwd's), the next
+ * call clears them, and a kernel whose wait ran out may have left out and lse
+ * partly written without the caller learning of it.
  * The scratch this kernel needs (two status words, 8 bytes) does not grow with
- * B, H, S or D; a need above ATTN_NOALLOC_SCRATCH_BYTES is rejected with
- * ATTN_ERR_INVALID_ARG before anything is enqueued.
+ * B, H, S or D.  The array's size is fixed when the library is built, and the
+ * build checks that the kernel's need fits it.
  *
  * The first call on a device sets that device up (looks up the device address
  * of the array with the device current); make that first call before any

@@ -56,14 +56,21 @@ __all__ = [
 _ROW_CHUNK = 1024
 
 
-def causal_mask(s_q: int, s_k: int) -> np.ndarray:
-    """Boolean [s_q, s_k] mask, True where a score is masked (key j > query i).
+def causal_mask(s_q: int, s_k: int, rows=None, cols=None) -> np.ndarray:
+    """Boolean mask, True where a score is masked (key j > query i).
 
-    "Math backend" section: ``ones → tril`` keeps the lower triangle.
+    "Math backend" section: ``ones → tril`` keeps the lower triangle, so
+    query i sees keys 0..i (top-left alignment when s_q != s_k).  The full
+    mask is [s_q, s_k]; ``rows`` (query indices in [0, s_q)) and ``cols``
+    (key indices in [0, s_k)) select a block of it without forming the rest.
     """
-    i = np.arange(s_q)[:, None]
-    j = np.arange(s_k)[None, :]
-    return j > i
+    i = np.arange(s_q) if rows is None else np.asarray(rows, dtype=np.int64)
+    j = np.arange(s_k) if cols is None else np.asarray(cols, dtype=np.int64)
+    if i.size and (i.min() < 0 or i.max() >= s_q):
+        raise ValueError("query rows must lie in [0, s_q)")
+    if j.size and (j.min() < 0 or j.max() >= s_k):
+        raise ValueError("key columns must lie in [0, s_k)")
+    return j[None, :] > i[:, None]
 
 
 def softmax_rows(scores: np.ndarray):
@@ -92,8 +99,7 @@ def _scores(q_rows: np.ndarray, k: np.ndarray, scale: float, causal: bool,
     s = q_rows @ k.T                      # step 1: q · kᵀ
     s = s * scale                         # step 2: · scale
     if causal:                            # step 3: masked_fill(mask, −inf)
-        j = np.arange(k.shape[0])[None, :]
-        s = np.where(j > row_index[:, None], -np.inf, s)
+        s = np.where(causal_mask(k.shape[0], k.shape[0], row_index), -np.inf, s)
     return s
 
 

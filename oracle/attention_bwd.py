@@ -28,7 +28,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import _head_rows, _scores, softmax_rows
+from .attention import _head_rows, _scores, causal_mask, softmax_rows
 
 __all__ = ["attention_bwd", "attention_bwd_rows"]
 
@@ -98,10 +98,9 @@ def attention_bwd_rows(q, k, v, dout, scale: float, causal: bool, b: int, h: int
     dz = attn * (dattn - delta[q_rows, None])
     dq = (dz * scale) @ kh
     # dk, dv rows: a column of attn over all queries
-    i = np.arange(S)[:, None]
     sc = (qh @ kh[kv_rows].T) * scale
     if causal:
-        sc = np.where(kv_rows[None, :] > i, -np.inf, sc)
+        sc = np.where(causal_mask(S, S, cols=kv_rows), -np.inf, sc)
     with np.errstate(invalid="ignore"):
         attn_c = np.where(live[:, None], np.exp(sc - lse[:, None]), 0.0)   # [S, n]
     dv = attn_c.T @ dh

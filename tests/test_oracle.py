@@ -18,7 +18,7 @@ import pytest
 import torch
 
 from oracle import (attention_fwd, attention_fwd_loops, attention_rows,
-                    attention_weights, softmax_rows)
+                    attention_weights, causal_mask, softmax_rows)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -298,3 +298,83 @@ def test_forward_mutant_harness_unmutated_passes():
 @pytest.mark.parametrize("kind", _FWD_MUTANTS)
 def test_forward_planted_mistake_fails_a_pin(kind):
     assert not _fwd_pins(_fwd_mutant(kind)), kind
+
+
+# ------------------------------------------------------------------ the causal mask
+# "Math backend" section of the profiling post: the mask is built as a matrix
+# of ones whose lower triangle is kept (tril), and the positions outside it
+# are filled with −inf.  The pins below rebuild that construction with
+# numpy's tril (a library routine, not the oracle's index comparison), spell
+# out one small case by hand, and check the row/column blocks the row forms
+# of the oracle use against the full mask.
+
+
+def _mask_pins(fn):
+    """The causal-mask pins as checks over an implementation; False if any fails."""
+    hand = np.array([[False, True, True],
+                     [False, False, True],
+                     [False, False, False]])
+    if not np.array_equal(fn(3, 3), hand):
+        return False
+    for s_q, s_k in ((1, 1), (1, 5), (5, 1), (4, 7), (7, 4), (16, 16)):
+        tril_kept = np.tril(np.ones((s_q, s_k), dtype=bool))
+        m = fn(s_q, s_k)
+        if m.shape != (s_q, s_k) or not np.array_equal(m, ~tril_kept):
+            return False
+    rows, cols = np.array([6, 0, 3]), np.array([5, 1, 6, 2])
+    full = fn(7, 7)
+    if not (np.array_equal(fn(7, 7, rows=rows), full[rows])
+            and np.array_equal(fn(7, 7, cols=cols), full[:, cols])
+            and np.array_equal(fn(7, 7, rows=rows, cols=cols), full[np.ix_(rows, cols)])):
+        return False
+    return True
+
+
+def test_causal_mask_is_the_complement_of_tril():
+    assert _mask_pins(causal_mask)
+
+
+def test_causal_mask_rejects_rows_outside_the_matrix():
+    with pytest.raises(ValueError):
+        causal_mask(4, 4, rows=[4])
+    with pytest.raises(ValueError):
+        causal_mask(4, 4, cols=[-1])
+
+
+def _mask_mutant(kind):
+    def fn(s_q, s_k, rows=None, cols=None):
+        i = np.arange(s_q) if rows is None else np.asarray(rows)
+        j = np.arange(s_k) if cols is None else np.asarray(cols)
+        if kind == "diagonal_masked":
+            return j[None, :] >= i[:, None]
+        if kind == "direction_reversed":
+            return j[None, :] < i[:, None]
+        if kind == "bottom_right_aligned":
+            return j[None, :] > i[:, None] + (s_k - s_q)
+        if kind == "rows_ignored":
+            return j[None, :] > np.arange(i.size)[:, None]
+        return j[None, :] > i[:, None]
+    return fn
+
+
+def test_mask_mutant_harness_unmutated_passes():
+    assert _mask_pins(_mask_mutant("none"))
+
+
+@pytest.mark.parametrize("kind", ["diagonal_masked", "direction_reversed", "bottom_right_aligned",
+                                  "rows_ignored"])
+def test_mask_planted_mistake_fails_a_pin(kind):
+    assert not _mask_pins(_mask_mutant(kind)), kind
+
+
+def test_forward_uses_the_pinned_mask(monkeypatch):
+    """The forward's step 3 goes through causal_mask: a slip planted there
+    shows up in the forward's own pins (brute force, hand-worked values)."""
+    import oracle.attention as oa
+    assert _fwd_pins(attention_fwd)
+    monkeypatch.setattr(oa, "causal_mask", _mask_mutant("diagonal_masked"))
+    q = np.arange(6, dtype=np.float64).reshape(1, 1, 3, 2) / 5
+    with np.errstate(invalid="ignore"):
+        out, _ = oa.attention_fwd(q, q, q, 1.0, True)
+    bo, _ = attention_fwd_loops(q.tolist(), q.tolist(), q.tolist(), 1.0, True)
+    assert not np.allclose(out, np.asarray(bo), equal_nan=False)
