@@ -24,6 +24,20 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxRegs = 200;
 constexpr int kControlRegs = 72;
 
+// The running max that serves as the exponent reference of a row is only
+// moved when a tile's max exceeds it by more than this many log2 units.  The
+// result is exact for any threshold (O and both sums share the reference);
+// the threshold bounds every p = 2^(t - m) by 2^threshold.  P must hold that
+// value: bf16 reaches 2^127, fp16 only 65504 < 2^16.  The fp32 sums then
+// stay finite while n_keys·2^threshold·max|v| < 2^128, i.e. for |v| < 2^65
+// at threshold 32 and any key count below 2^31.  Rounding is relative, so
+// the reference's distance from the true max costs no precision; and the
+// reference never exceeds the true max, so no p underflows earlier than with
+// the exact max.  A high threshold makes moves (a redo of the tile's
+// exponentials and a rescale of O in TMEM) rare even for peaked softmaxes.
+template <bool F16>
+constexpr float kRescaleThreshold = F16 ? 8.0f : 32.0f;
+
 struct FwdParams {
   CUtensorMap tm_q;  // q as (D, S, B·H), box 64 x 128 rows, 128-byte swizzle
   CUtensorMap tm_k;  // k, same box

@@ -17,10 +17,10 @@
 // first BN/2), Q [2·BN, 2·BN + D/2) (two 16-bit values per column), O in the
 // last D.  The softmax computes its exponentials against the running
 // reference before the tile's max is known and redoes them only when the tile
-// moves the reference by more than 2^8.  At D = 256 two Q tiles' accumulators
-// would fill TMEM on their own; at D = 128 this layout runs the causal case
-// (the two-tile kernel stays faster when the reference moves often, as under a
-// peaked non-causal softmax).
+// moves the reference by more than the threshold of attn_fwd.h (2^32 for
+// bf16, 2^8 for fp16).  At D = 256 two Q tiles' accumulators would fill TMEM
+// on their own; at D = 128 this layout runs the causal case (the two-tile
+// kernel is faster without the mask).
 //
 // Roles (192 threads): warps 0-3 softmax / correction / epilogue, one thread
 // per query row (TMEM lane); warp 4 issues tcgen05.mma and owns TMEM; warp 5
@@ -39,7 +39,6 @@ namespace {
 constexpr int kQRows = 128;                      // rows of the Q tile
 constexpr int kThreads1Q = 192;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;        // log2 units, as in the two-tile kernel
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
 // D: head dimension; BN: rows of one K/V tile
@@ -228,7 +227,7 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
       bool moved = false;
       if (m == -INFINITY) {
         m = m_tile;  // first tile with an allowed key sets the reference
-      } else if (m_tile > m + kRescaleThreshold) {
+      } else if (m_tile > m + kRescaleThreshold<F16>) {
         alpha = ex2_approx(m - m_tile);
         m = m_tile;
         moved = true;

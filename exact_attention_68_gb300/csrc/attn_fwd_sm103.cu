@@ -11,8 +11,9 @@
 // sequence (one CTA per (b, h, 256 query rows)), §1 the softmax does as few
 // non-matmul operations as it can (exp2 with the scale folded in, the 1/l
 // normalisation deferred to the end, and the running max only moved when it
-// grows by more than 2^8, which keeps every exponent ≤ 8 and is exact because
-// the same reference max scales both O and l).
+// grows by more than the threshold of attn_fwd.h, which bounds every exponent
+// by that threshold and is exact because the same reference max scales both
+// O and l).
 //
 // GB300 mapping (one CTA per SM: 225 KB of shared memory, all 512 TMEM columns):
 //   warps 0-3   softmax/correction/epilogue for Q tile 0 (rows 0-127 of the unit)
@@ -47,8 +48,6 @@ namespace ea {
 namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
-// The running max is only moved when it grows by more than this (log2 units).
-constexpr float kRescaleThreshold = 8.0f;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // bound on waits while tearing down
 
 template <int D>
@@ -258,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       bool moved = false;
       if (j == 0) {
         m = m_tile;  // first tile: the reference is this tile's max
-      } else if (m_tile > m + kRescaleThreshold) {
+      } else if (m_tile > m + kRescaleThreshold<F16>) {
         alpha = ex2_approx(m - m_tile);
         m = m_tile;
         moved = true;

@@ -96,6 +96,30 @@ def test_peaked_softmax_many_rescales(cuda_device):
         compare(to_f64(out), to_f64(lse), ro, rl, f"peaked causal={causal}")
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_reference_moves_on_every_tile(cuda_device, D):
+    """Logits built to climb by about 40 log2 units from each 128-key tile to
+    the next, so every row's reference max moves (by more than the bf16
+    threshold of 32) on every tile, with the rescale of O and the redo of the
+    tile's exponentials each time; the within-tile spread keeps the softmax
+    from collapsing onto a single key."""
+    S = 1024
+    g = torch.Generator().manual_seed(17)
+    q = torch.randn(1, 2, S, D, generator=g) * 0.5
+    k = torch.randn(1, 2, S, D, generator=g) * 0.5
+    v = torch.randn(1, 2, S, D, generator=g)
+    scale = default_scale(D)
+    # coordinate 0 carries the climb: s_ij gains q_i0 * k_j0 * scale
+    q[..., 0] = 4.0
+    step = 40.0 / 1.4426950408889634 / (4.0 * scale)  # +40 log2 units per tile
+    k[..., 0] = step * (torch.arange(S) // 128).float()
+    q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
+    for causal in (True, False):
+        out, lse = run_gpu(q, k, v, scale, causal)
+        ro, rl = attention_fwd(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, causal)
+        compare(to_f64(out), to_f64(lse), ro, rl, f"moving reference D={D} causal={causal}")
+
+
 def test_constant_v_closed_form(cuda_device):
     """Every V row equal to c gives out = c (rounded to bf16) for every row."""
     q, k, _ = make_qkv((1, 2, 777, 128), seed=8)
