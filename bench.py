@@ -38,17 +38,17 @@ WORKLOAD = "c5"
 # The forward kernels' device code (the one-Q-tile kernel runs the causal
 # D=128 workload, the two-tile kernel the non-causal and D=64 side workloads)
 # and the two-tile kernel's grid schedule (schedule.h).
-KERNEL_SOURCES = ["exact_attention_68_gb300/csrc/attn_fwd_1q_sm103.cu",
-                  "exact_attention_68_gb300/csrc/attn_fwd_sm103.cu",
+KERNEL_SOURCES = ["exact_attention_68_gb300/csrc/attn_fwd_1qp_sm103.cu",
+                  "exact_attention_68_gb300/csrc/attn_fwd_1q_sm103.cu",
                   "exact_attention_68_gb300/csrc/ptx.cuh", "exact_attention_68_gb300/csrc/umma.cuh",
                   "exact_attention_68_gb300/csrc/attn_fwd.h", "exact_attention_68_gb300/csrc/schedule.h"]
 # DRAM bytes (read + write) per launch of the forward kernel on the default
 # workload, from ncu captures, keyed by the hash of the kernel sources they
 # were taken on (a changed kernel reports null until captured again).
 NCU_TRAFFIC_BYTES = {
-    # B=1 H=32 S=16384 D=128 causal (attn_fwd_1q_kernel<128,128,true>):
-    # 597,567,744 read + 118,328,576 written
-    "b39b5f0eff5bd4af": 715896320,
+    # B=1 H=32 S=16384 D=128 causal (attn_fwd_1qp_kernel<128,true,bf16>):
+    # 601,260,800 read + 117,115,648 written
+    "6c260678af76fa23": 718376448,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -458,7 +458,7 @@ def run_ours(args, world, rank, local):
                      # the regime of the sustained cuBLAS figure
                      "peak_sustained": float(peaks.get("bf16_tflops_sustained", peak)),
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
-                     "kernel": "attn_fwd_1q_kernel<128,128,true>",
+                     "kernel": "attn_fwd_1qp_kernel<128,true,bf16>",
                      "algorithmic_flops_per_launch": flops,
                      "algorithmic_bytes_per_launch": algorithmic_bytes(w.B, w.H, w.S, w.D)},
         "e2e": {"value": flops * e2e_steps / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",

@@ -79,9 +79,7 @@ attn_status_t validate(const void* q, const void* k, const void* v, const void* 
   const int64_t BH = B * H;  // < 2^62, no overflow
   if (BH > INT32_MAX) return ATTN_ERR_INVALID_ARG;
   const int64_t n_qt = (S + ea::kBlockM - 1) / ea::kBlockM;
-  const int64_t n_units = (n_qt + ea::kQTilesPerUnit - 1) / ea::kQTilesPerUnit;
-  if (BH * n_units > INT32_MAX) return ATTN_ERR_INVALID_ARG;
-  if (BH * n_qt > INT32_MAX) return ATTN_ERR_INVALID_ARG;  // one CTA per Q tile
+  if (BH * n_qt > INT32_MAX) return ATTN_ERR_INVALID_ARG;  // one grid CTA per Q tile
   if (BH > (int64_t(1) << 62) / (S * D * 2)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out)) & 15u)
@@ -167,61 +165,35 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
   // so TMA loads read zeros past it and stores leave those columns out; the
   // zero columns add nothing to q·kᵀ and give zero output columns.
   const int dk = kernel_head_dim(D);
-  // One Q tile per CTA for 256 columns, and for causal 128 (measured faster
-  // there); the two-tile kernel otherwise.
-  if (dk == 256 || (dk == 128 && causal != 0)) {
-    const int bn = dk == 256 ? 64 : 128;  // rows of one K/V tile
-    Fwd1QParams p;
-    std::memset(&p, 0, sizeof(p));
-    if (!encode_bhsd_16bit(&p.tm_k, k, BH, S, D, bn, f16) ||
-        !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, bn, f16) ||
-        !encode_bhsd_16bit(&p.tm_o, out, BH, S, D, 32, f16))
-      return cuda_failure(kErrTensorMap);
-    p.q = static_cast<const uint16_t*>(q);
-    p.lse = lse;
-    p.status = status;
-    p.BH = static_cast<int>(BH);
-    p.S = static_cast<int>(S);
-    p.d_cols = static_cast<int>(D);
-    p.n_qt = static_cast<int>((S + 127) / 128);
-    p.n_kt = static_cast<int>((S + bn - 1) / bn);
-    int dev1 = 0, sms1 = 0;
-    cudaError_t e1 = cudaGetDevice(&dev1);
-    if (e1 == cudaSuccess) e1 = cudaDeviceGetAttribute(&sms1, cudaDevAttrMultiProcessorCount, dev1);
-    if (e1 != cudaSuccess) return cuda_failure(static_cast<int>(e1));
-    p.sched = plan_schedule(BH, p.n_qt, S, D, causal != 0, kL2GroupBytes, sms1);
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    p.timeout_ns = timeout_ns;
-    const cudaError_t e = fwd1q_launch(p, dk, causal != 0, f16, stream);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();
-      return cuda_failure(static_cast<int>(e));
-    }
-    return ATTN_OK;
-  }
-  FwdParams p;
+  // 64 and 128 columns: the persistent kernel (one CTA per SM walking Q
+  // tiles); 256 columns: one Q tile per CTA with 64-row K/V tiles (its output
+  // tile does not fit the persistent kernel's staging buffer).
+  const bool persistent = dk <= 128;
+  const int bn = dk == 256 ? 64 : 128;  // rows of one K/V tile
+  Fwd1QParams p;
   std::memset(&p, 0, sizeof(p));
-  if (!encode_bhsd_16bit(&p.tm_q, q, BH, S, D, kBlockM, f16) ||
-      !encode_bhsd_16bit(&p.tm_k, k, BH, S, D, kBlockN, f16) ||
-      !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, kBlockN, f16) ||
-      !encode_bhsd_16bit(&p.tm_o, out, BH, S, D, 32, f16))
+  if (!encode_bhsd_16bit(&p.tm_k, k, BH, S, D, bn, f16) ||
+      !encode_bhsd_16bit(&p.tm_v, v, BH, S, D, bn, f16) ||
+      !encode_bhsd_16bit(&p.tm_o, out, BH, S, D, 32, f16) ||
+      !encode_bhsd_16bit(&p.tm_q, q, BH, S, D, 128, f16))
     return cuda_failure(kErrTensorMap);
+  p.q = static_cast<const uint16_t*>(q);
   p.lse = lse;
   p.status = status;
-  p.B = static_cast<int>(B);
-  p.H = static_cast<int>(H);
+  p.BH = static_cast<int>(BH);
   p.S = static_cast<int>(S);
   p.d_cols = static_cast<int>(D);
   p.n_qt = static_cast<int>((S + kBlockM - 1) / kBlockM);
-  p.n_units = (p.n_qt + kQTilesPerUnit - 1) / kQTilesPerUnit;
+  p.n_kt = static_cast<int>((S + bn - 1) / bn);
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_failure(static_cast<int>(e));
-  p.sched = plan_schedule(BH, p.n_units, S, D, causal != 0, kL2GroupBytes, sms);
+  p.sched = plan_schedule(BH, p.n_qt, S, D, causal != 0, kL2GroupBytes, sms);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout_ns;
-  e = fwd_launch(p, dk, causal != 0, f16, stream);
+  e = persistent ? fwd1qp_launch(p, dk, causal != 0, f16, stream)
+                 : fwd1q_launch(p, dk, causal != 0, f16, stream);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return cuda_failure(static_cast<int>(e));

@@ -11,18 +11,8 @@
 
 namespace ea {
 
-// Rows of one Q tile (the tcgen05 M) and of one K/V tile.
+// Rows of one Q tile (the tcgen05 M).
 constexpr int kBlockM = 128;
-constexpr int kBlockN = 128;
-// Q tiles per CTA work unit (two softmax warpgroups ping-pong on the tensor core).
-constexpr int kQTilesPerUnit = 2;
-// Warps 0-7: two softmax warpgroups; warps 8-11: control warpgroup (warp 8 MMA
-// issuer, warp 9 TMA producer, warps 10-11 idle).
-constexpr int kThreads = 384;
-// Register split set with setmaxnreg; launch budget 384 x 168 = 64512 >=
-// 256 x 200 + 128 x 72 = 60416.
-constexpr int kSoftmaxRegs = 200;
-constexpr int kControlRegs = 72;
 
 // The running max that serves as the exponent reference of a row is only
 // moved when a tile's max exceeds it by more than this many log2 units.  The
@@ -38,28 +28,13 @@ constexpr int kControlRegs = 72;
 template <bool F16>
 constexpr float kRescaleThreshold = F16 ? 8.0f : 32.0f;
 
-struct FwdParams {
-  CUtensorMap tm_q;  // q as (D, S, B·H), box 64 x 128 rows, 128-byte swizzle
-  CUtensorMap tm_k;  // k, same box
-  CUtensorMap tm_v;  // v, same box
-  CUtensorMap tm_o;  // out, box 64 x 32 rows (one warp's rows), 128-byte swizzle
-  float* lse;        // [B·H, S]
-  int* status;       // device status word pair (error bits, first wait site)
-  int B, H, S;
-  int d_cols;        // the tensors' head dimension (<= D, a multiple of 8)
-  int n_qt;          // ceil(S / 128)
-  int n_units;       // ceil(n_qt / 2): work units per (b, h)
-  UnitSchedule sched;  // CTA index -> (b·H + h, unit level)
-  float scale_log2;  // scale · log2(e)
-  uint64_t timeout_ns;
-};
-
-// The one-Q-tile kernel: one 128-row Q tile per CTA, Q in TMEM, BN-row K/V
-// tiles (BN = 64 at D = 256, 128 at D = 128).
+// Parameters of the forward kernels: one 128-row Q tile at a time, Q in TMEM,
+// BN-row K/V tiles (BN = 64 at D = 256, else 128).
 struct Fwd1QParams {
   CUtensorMap tm_k;    // k as (D, S, B·H), box 64 x BN rows, 128-byte swizzle
   CUtensorMap tm_v;    // v, same box
   CUtensorMap tm_o;    // out, box 64 x 32 rows
+  CUtensorMap tm_q;    // q, box 64 x 128 rows: L2 prefetch of a Q tile (persistent kernel)
   const uint16_t* q;   // 16-bit [B·H, S, d_cols]: rows read into TMEM
   float* lse;          // [B·H, S]
   int* status;
@@ -74,14 +49,12 @@ struct Fwd1QParams {
 };
 
 // One Q tile per CTA, Q in TMEM: D = 256 (64-row K/V tiles) and D = 128
-// (128-row K/V tiles).
+// (128-row K/V tiles).  The library runs D = 256 on it.
 cudaError_t fwd1q_launch(const Fwd1QParams& p, int D, bool causal, bool f16, cudaStream_t stream);
 
-// Dynamic shared memory one CTA of the D-specialised kernel uses.
-size_t fwd_smem_bytes(int D);
-
-// Sets per-kernel attributes (once per device) and launches one forward.
-// f16: q, k, v, out are fp16 (else bf16).
-cudaError_t fwd_launch(const FwdParams& p, int D, bool causal, bool f16, cudaStream_t stream);
+// The same computation with one CTA per SM walking Q tiles (D = 64 or 128):
+// a running CTA takes over the Q tile of the next CTA of the grid that has not
+// been launched yet, so the next tile's start overlaps this tile's end.
+cudaError_t fwd1qp_launch(const Fwd1QParams& p, int D, bool causal, bool f16, cudaStream_t stream);
 
 }  // namespace ea

@@ -1,5 +1,6 @@
 // attn_fwd_1q_sm103.cu — the fused attention forward with one Q tile per CTA
-// on GB300 (sm_103a): head dimension 256, and 128 under the causal mask.
+// on GB300 (sm_103a), for head dimension 256 (the persistent kernel runs the
+// narrower ones).
 //
 // Same computation as the D = 64 / 128 kernel: out = softmax(scale·q·kᵀ +
 // causal mask)·v per (batch, head) with the row logsumexp, following the five
@@ -19,8 +20,8 @@
 // reference before the tile's max is known and redoes them only when the tile
 // moves the reference by more than the threshold of attn_fwd.h (2^32 for
 // bf16, 2^8 for fp16).  At D = 256 two Q tiles' accumulators would fill TMEM
-// on their own; at D = 128 this layout runs the causal case (the two-tile
-// kernel is faster without the mask).
+// on their own, and the 64 KB output tile does not fit beside the K/V rings,
+// so this kernel is not persistent.
 //
 // Roles (192 threads): warps 0-3 softmax / correction / epilogue, one thread
 // per query row (TMEM lane); warp 4 issues tcgen05.mma and owns TMEM; warp 5
@@ -104,6 +105,25 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
   int nkv = CAUSAL ? (i + 1) * (kQRows / BN) : p.n_kt;  // K/V tiles this Q tile meets
   if (nkv > p.n_kt) nkv = p.n_kt;
 
+  // A softmax thread's row of Q, requested before the set-up below so that
+  // the load's latency overlaps it: all of the row's 16-byte loads are in
+  // flight at once (rows past S and columns past d_cols load nothing and
+  // hold zero).  It goes into TMEM once the allocation exists.
+  uint32_t qw[kD / 2];
+  if (warp < 4) {
+    const int grow = i * kQRows + warp * 32 + lane;
+    const bool valid = grow < p.S;
+    const uint16_t* qr = p.q + (valid ? (int64_t)bh * p.S + grow : 0) * p.d_cols;
+#pragma unroll
+    for (int u = 0; u < kD / 8; ++u) {
+      const int col = 8 * u;
+      const uint4 x = valid && col < p.d_cols && dbg_row(dbb, bh, grow, col, 8, kChkQLoad)
+                          ? __ldg(reinterpret_cast<const uint4*>(qr + col))
+                          : make_uint4(0u, 0u, 0u, 0u);
+      qw[4 * u] = x.x, qw[4 * u + 1] = x.y, qw[4 * u + 2] = x.z, qw[4 * u + 3] = x.w;
+    }
+  }
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kKFull + s), 1);
@@ -143,23 +163,11 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
     const uint32_t tO = tmem_base + lane_bits + kOCol;
     {
       // this row of Q into TMEM, 32 columns (64 values) per store
-      // (rows past S and columns past d_cols load nothing and hold zero)
-      const int64_t qrow = valid ? (int64_t)bh * p.S + grow : 0;
-      const uint16_t* qr = p.q + qrow * p.d_cols;
 #pragma unroll
-      for (int c = 0; c < kD / 64; ++c) {
-        uint32_t w[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int col = 64 * c + 8 * u;
-          const uint4 x = valid && col < p.d_cols && dbg_row(dbb, bh, grow, col, 8, kChkQLoad)
-                              ? __ldg(reinterpret_cast<const uint4*>(qr + col))
-                              : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * u] = x.x, w[4 * u + 1] = x.y, w[4 * u + 2] = x.z, w[4 * u + 3] = x.w;
-        }
+      for (int c = 0; c < kD / 64; ++c)
         if (dbg_warp(dbg_tmem(dbb, tmem_base + lane_bits + kQCol + 32 * c, 32, warp, kChkQTmem)))
-          tmem_st_32x32b_x32(tmem_base + lane_bits + kQCol + 32 * c, w);
-      }
+          tmem_st_32x32b_x32(tmem_base + lane_bits + kQCol + 32 * c,
+                             *reinterpret_cast<const uint32_t(*)[32]>(&qw[32 * c]));
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(kQTmem));
@@ -276,23 +284,27 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
     if (ok) {
       tc_fence_after_sync();
       const float inv_l = lq > 0.f ? 1.f / lq : 0.f;
-      // 4 column blocks of 64 (128 bytes per row), 128 rows each (16 KB)
+      // column blocks of 64 (128 bytes per row), 128 rows each (16 KB); the
+      // two 32-column loads of a block are in flight together
 #pragma unroll 1
-      for (int c = 0; c < kD / 32 && dbg_warp(dbg_tmem(dbb, tO + 32 * c, 32, warp, kChkOTmem)); ++c) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tO + 32 * c, o);
+      for (int c2 = 0; c2 < kD / 64 && dbg_warp(dbg_tmem(dbb, tO + 64 * c2, 64, warp, kChkOTmem));
+           ++c2) {
+        uint32_t o[2][32];
+        tmem_ld_32x32b_x32(tO + 64 * c2, o[0]);
+        tmem_ld_32x32b_x32(tO + 64 * c2 + 32, o[1]);
         tmem_ld_wait();
-        reg_fence(o);
+        reg_fence(o[0]);
+        reg_fence(o[1]);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int unit = (c & 1) * 4 + q4;  // 16-byte unit within the 128-byte row
-          const uint32_t addr = sb + kKOff + (c >> 1) * (kQRows * 128) + row * 128 +
+        for (int unit = 0; unit < 8; ++unit) {  // 16-byte unit within the 128-byte row
+          const uint32_t addr = sb + kKOff + c2 * (kQRows * 128) + row * 128 +
                                 ((unit ^ (row & 7)) << 4);
+          const uint32_t* src = &o[unit >> 2][(unit & 3) * 8];
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            w[e] = pack_x2<F16>(__uint_as_float(o[q4 * 8 + 2 * e]) * inv_l,
-                                __uint_as_float(o[q4 * 8 + 2 * e + 1]) * inv_l);
+            w[e] = pack_x2<F16>(__uint_as_float(src[2 * e]) * inv_l,
+                                __uint_as_float(src[2 * e + 1]) * inv_l);
           if (dbg_smem(dbb, addr, 16, 16, kChkStage)) st_shared_v4(addr, w[0], w[1], w[2], w[3]);
         }
       }
@@ -456,10 +468,6 @@ cudaError_t launch_1q(const Fwd1QParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t fwd1q_launch(const Fwd1QParams& p, int D, bool causal, bool f16, cudaStream_t stream) {
-  if (D == 128) {
-    if (f16) return causal ? launch_1q<128, 128, true, true>(p, stream) : launch_1q<128, 128, false, true>(p, stream);
-    return causal ? launch_1q<128, 128, true, false>(p, stream) : launch_1q<128, 128, false, false>(p, stream);
-  }
   if (D != 256) return cudaErrorInvalidValue;
   if (f16) return causal ? launch_1q<256, 64, true, true>(p, stream) : launch_1q<256, 64, false, true>(p, stream);
   return causal ? launch_1q<256, 64, true, false>(p, stream) : launch_1q<256, 64, false, false>(p, stream);

@@ -1,9 +1,9 @@
 // schedule.h — which work unit each CTA of the forward kernel's 1-D grid takes.
 //
-// A work unit is one (b·H + h) slice and one pair of 128-row Q tiles, unit
-// level u covering Q tiles 2u and 2u+1.  Under the causal mask level u does
-// 2u+2 KV tile-steps, so the levels differ in cost and the order of the grid
-// decides both the load balance and how often K/V tiles come back from DRAM:
+// A work unit is one (b·H + h) slice and one 128-row Q tile: unit level u is
+// Q tile u.  Under the causal mask level u does u+1 K/V tile-steps (of 128
+// keys), so the levels differ in cost and the order of the grid decides both
+// the load balance and how often K/V tiles come back from DRAM:
 //
 //   phase 1  levels n_units-1 .. tail_levels, one group of heads_per_group
 //            slices at a time; within a group the levels go heaviest first and

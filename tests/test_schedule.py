@@ -2,7 +2,7 @@
 
 The map is compiled from the kernel's own header into a host-only shim; the
 checks need no GPU.  A work unit is one (b·H + h) slice and one unit level u
-(Q tiles 2u, 2u+1); under the causal mask level u costs 2u+2 KV tile-steps.
+(Q tile u); under the causal mask level u costs u+1 KV tile-steps.
 """
 import ctypes
 import itertools
@@ -107,10 +107,13 @@ def test_plan_rules(shim, BH, S, D, causal):
 
 def test_plan_long_context_causal(shim):
     # B=1, H=32, S=16384, D=128: 8 MiB of K/V per slice -> 6 slices per group;
-    # 64 unit levels, sqrt(2 * 64 * 152 / 32) = 24.7 -> 25 levels in phase 2
-    assert _plan(shim, 32, 64, 16384, 128, True) == (6, 25)
-    # B=2, H=16, S=4096, D=128: 2 MiB per slice -> 24 per group, 13 tail levels
-    assert _plan(shim, 32, 16, 4096, 128, True) == (24, 13)
+    # 128 Q tiles, sqrt(2 * 128 * 152 / 32) = 34.9 -> 35 levels in phase 2
+    assert _plan(shim, 32, 128, 16384, 128, True) == (6, 35)
+    # B=2, H=16, S=4096, D=128: 2 MiB per slice -> 24 per group; 32 Q tiles,
+    # sqrt(2 * 32 * 152 / 32) = 17.4 -> 18 tail levels
+    assert _plan(shim, 32, 32, 4096, 128, True) == (24, 18)
+    # without the mask every unit costs the same: no phase 2
+    assert _plan(shim, 128, 16, 2048, 128, False) == (48, 0)
 
 
 @pytest.mark.parametrize("BH", [1, 2, 7, 13, 18, 32, 100])
