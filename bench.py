@@ -7,10 +7,13 @@ causal workload B=1, H=32, S=16384, D=128 (bf16 in, fp32 accumulate, bf16 out
 + fp32 lse), inputs resident in HBM.  The inputs (403 MB) exceed the 129 MB L2,
 so no flush is needed between steps.  Prints one JSON line (rank 0).
 
-Under torchrun (N > 1) every rank runs its own replica of the workload on its
-own GPU (the path shards by (batch, head) with no exchange step), timing is
-bracketed by a barrier + synchronize on both sides and the max over ranks is
-taken ("scaling": "weak").
+Under torchrun (N > 1) the job is one global problem of N times the
+workload's batch, split by (batch, head) slices over the ranks with
+attn_shard_range (one process per GPU, no exchange step: every slice is
+independent); rank r holds batch block r, drawn with seed r, so rank 0's
+inputs are the N = 1 workload's.  Timing is bracketed by a barrier +
+synchronize on both sides and the max over ranks is taken ("scaling":
+"weak": the work per GPU is fixed).
 
 --impl reference times the fp64 CPU oracle on the host cores instead (each
 step a bounded sample of query rows of the same workload), rank 0 only.
@@ -75,7 +78,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi every 200 ms."""
+    """Samples SM clocks and throttle reasons with nvidia-smi every 20 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -86,7 +89,7 @@ class ClockSampler:
         self.proc = None
         self.thread = None
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", "20"]
         if gpu_id:
             cmd += ["-i", gpu_id]
         try:
@@ -205,6 +208,16 @@ def oracle_rows_sample(qn, kn, vn, scale, causal, rows_per_head, heads, budget_s
     return flops / secs / 1e12, done, secs
 
 
+def bench_config(w, world, scale):
+    """The `config` of the JSON line (the same for both arms)."""
+    return {"workload": w.about, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
+            "global_batch": w.B * world, "scale": scale,
+            "seed": "rank r holds batch block r, drawn with seed r (rank 0: seed 0)",
+            "l2": "inputs 403 MB > 129 MB L2: no flush between steps",
+            "parallelism": f"head-sharded x{world}: the global problem's (b, h) slices split "
+                           "contiguously over the ranks (attn_shard_range), no collective"}
+
+
 def run_reference(args, world, rank):
     """The oracle on the host cores: `steps` timed samples after `warmup` untimed ones."""
     if rank != 0:
@@ -212,7 +225,7 @@ def run_reference(args, world, rank):
     w = WORKLOADS[WORKLOAD]
     qn, kn, vn = as_numpy(*make_qkv(w, seed=0))
     scale = default_scale(w.D)
-    rows_per_step = 32
+    rows_per_step = 256  # the same per-head sample as the cpu_baseline leg of the other arm
     for i in range(args.warmup):
         oracle_rows_sample(qn, kn, vn, scale, w.causal, rows_per_step, [i % w.H], 1e9)
     flops, t0 = 0, time.perf_counter()
@@ -223,14 +236,13 @@ def run_reference(args, world, rank):
     secs = time.perf_counter() - t0
     val = flops / secs / 1e12
     cores = len(os.sched_getaffinity(0))
-    sample = (f"{rows_per_step} evenly spaced query rows of one head per step (head = step mod 32) "
+    sample = (f"{rows_per_step} evenly spaced query rows of one head per step (head = step mod {w.H}) "
               f"of the {w.about} workload; oracle row form, fp64 numpy")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / max(args.steps, 1) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.about, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
-                       "causal": w.causal},
+            "config": bench_config(w, world, scale),
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -266,12 +278,69 @@ def executed_flops(B, H, S, D, causal):
 
 
 def blas_threads():
+    """(threads, how it was found) of the BLAS numpy calls."""
     try:
         from threadpoolctl import threadpool_info
-        return max((i.get("num_threads", 0) for i in threadpool_info()), default=None)
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return n, "threadpoolctl"
     except Exception:
-        v = os.environ.get("OMP_NUM_THREADS")
-        return int(v) if v and v.isdigit() else None
+        pass
+    # no threadpoolctl: ask the OpenBLAS numpy loaded (its library is mapped
+    # into this process) through its exported thread-count query
+    import ctypes
+    np.dot(np.ones((2, 2)), np.ones((2, 2)))  # make sure BLAS is loaded
+    try:
+        with open("/proc/self/maps") as f:
+            libs = sorted({ln.split()[-1] for ln in f if "openblas" in ln.lower() and ".so" in ln})
+    except OSError:
+        libs = []
+    for path in libs:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                    "scipy_openblas_get_num_threads", "openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn()), f"{sym} ({os.path.basename(path)})"
+    v = os.environ.get("OMP_NUM_THREADS")
+    if v and v.isdigit():
+        return int(v), "OMP_NUM_THREADS"
+    return os.cpu_count(), "os.cpu_count (no BLAS thread query available)"
+
+
+def oracle_per_config(budget_s, full_cap_s=30.0):
+    """Wall time of the fp64 oracle on c1-c4.  c1 runs whole.  c2-c4 are first
+    timed on evenly spaced rows of every head for about `budget_s` seconds;
+    c2 and c4 then run whole if that rate puts the whole problem under
+    `full_cap_s`, and c3 (like c5, the cpu_baseline) keeps the time
+    extrapolated from the rate in counted FLOPs, flagged as such."""
+    from oracle import attention_fwd
+    res = {}
+    for name in ("c1", "c2", "c3", "c4"):
+        w = WORKLOADS[name]
+        qn, kn, vn = as_numpy(*make_qkv(w, seed=0))
+        scale = default_scale(w.D)
+        total = counted_flops(w.B, w.H, w.S, w.D, w.causal)
+        rows = w.B * w.H * w.S
+        est = None
+        if name != "c1":
+            tf, n_rows, secs = oracle_rows_sample(qn, kn, vn, scale, w.causal, min(w.S, 256),
+                                                  list(range(w.H)), budget_s)
+            est = total / (tf * 1e12)
+            if name == "c3" or est > full_cap_s:
+                res[name] = {"rows": n_rows, "s": secs, "tflops": tf, "full_s": est,
+                             "extrapolated": True}
+                continue
+        t0 = time.perf_counter()
+        attention_fwd(qn, kn, vn, scale, w.causal)
+        secs = time.perf_counter() - t0
+        res[name] = {"rows": rows, "s": secs, "tflops": total / secs / 1e12, "full_s": secs,
+                     "extrapolated": False, "sample_estimate_s": est}
+    return res
 
 
 def side_workloads(device, stream):
@@ -363,8 +432,13 @@ def run_ours(args, world, rank, local):
         B, H, S, D = (int(x) for x in args.shape.split(","))
         w = Workload("shape", B, H, S, D, True, about=f"causal B={B} H={H} S={S} D={D}, N(0,1)")
     scale = default_scale(w.D)
-    flops = counted_flops(w.B, w.H, w.S, w.D, w.causal)
-    q_h, k_h, v_h = (x.pin_memory() for x in make_qkv(w, seed=0))
+    flops = counted_flops(w.B, w.H, w.S, w.D, w.causal)  # per rank
+    # this rank's share of the global problem (world batch blocks of w.B
+    # elements): world divides the slices evenly, so it is batch block `rank`
+    units = w.B * w.H * world
+    first, count = binding.shard_range(units, world, rank)
+    assert (first, count) == (rank * w.B * w.H, w.B * w.H), (first, count)
+    q_h, k_h, v_h = (x.pin_memory() for x in make_qkv(w, seed=rank))
     q, k, v = (x.to(device) for x in (q_h, k_h, v_h))
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=device)
@@ -394,6 +468,18 @@ def run_ours(args, world, rank, local):
     status = binding.device_status(device)
     ms_max = reduce_max(ms, world, device)
     clk = clocks.summary(t0, t1)
+    # clock check: the same step back to back for about a second (not part of
+    # the value), long enough for several clock samples; its per-launch time
+    # times the median SM clock gives the cycles a launch takes
+    n_chk = max(10, int(1000.0 / max(ms / args.steps, 1e-3)))
+    c0 = time.time()
+    chk_ms = time_steps(step, n_chk, stream) / n_chk
+    c1 = time.time()
+    chk = clocks.summary(c0, c1)
+    clock_check = {"launches": n_chk, "ms_per_launch": chk_ms, "sm_mhz_median": chk["sm_mhz"],
+                   "reasons": chk["reasons"], "samples": chk["samples"],
+                   "mcycles_per_launch": (chk_ms * 1e-3 * chk["sm_mhz"] * 1e6 / 1e6
+                                          if chk["sm_mhz"] else None)}
 
     # end to end: host inputs (pinned) -> device -> kernel -> host outputs, per step
     out_h = torch.empty_like(q_h).pin_memory()
@@ -430,12 +516,15 @@ def run_ours(args, world, rank, local):
         checked = []
         tf, n_rows, secs = oracle_rows_sample(*as_numpy(q_h, k_h, v_h), scale, w.causal, 256,
                                               list(range(w.H)), args.cpu_budget, checked)
+        nthr, how = blas_threads()
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-               "kind": "oracle", "blas_threads": blas_threads(),
+               "kind": "oracle", "blas_threads": nthr, "blas_threads_source": how,
                "full_problem_s_extrapolated": flops / (tf * 1e12),
                "sample": f"{n_rows} query rows (256 evenly spaced per head, heads in order) of the "
                          f"{w.about} workload, oracle row form in fp64 numpy, {secs:.1f} s"}
         extra["parity"] = parity_of_outputs(checked, out_h, lse_h)
+        if not args.no_side:
+            extra["oracle_per_config"] = oracle_per_config(args.cpu_budget / 4)
     if rank != 0:
         return
     nb = w.B * w.H * w.S * w.D * 2
@@ -443,10 +532,8 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.about, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
-                   "scale": scale, "seed": 0,
-                   "l2": "inputs 403 MB > 129 MB L2: no flush between steps",
-                   "parallelism": f"replicas x{world} (independent (b,h) shards)"},
+        "config": bench_config(w, world, scale),
+        "shard": {"rank": rank, "world": world, "first": first, "count": count, "units": units},
         "pct_of_peak": 100.0 * achieved / peak,
         "ms_per_launch": {"mean": ms_max / args.steps, "median": statistics.median(per_launch),
                           "min": min(per_launch), "max": max(per_launch)},
@@ -466,6 +553,7 @@ def run_ours(args, world, rank, local):
                 "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps},
         "gpu_launches": args.steps,
         "clocks": clk,
+        "clock_check": clock_check,
         "device_status": status,
         "cpu_baseline": cpu,
         "kernel_hash": kernel_hash(),

@@ -19,6 +19,7 @@ from .build import LIB_PATH
 
 __all__ = ["AttnError", "load_library", "attn_fwd", "attn_fwd_bounded", "attn_fwd_staged",
            "attn_fwd_noalloc", "attn_bwd", "attn_bwd_bounded", "attention", "device_status",
+           "shard_range", "attn_fwd_sharded",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
            "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_ERR_DEVICE_CHECK", "ATTN_BF16", "ATTN_F16", "EXPORTED_SYMBOLS"]
 
@@ -43,6 +44,7 @@ _SIGS = {
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_abi_version": (_i, []),
     "attn_last_cuda_error": (_i, []),
+    "attn_shard_range": (_i, [_i64, _i, _i, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -284,6 +286,50 @@ def device_status(device=None, stream=None) -> int:
     lib = load_library()
     with torch.cuda.device(dev):
         return int(lib.attn_device_status(_stream_handle(dev, stream)))
+
+
+def shard_range(units: int, world: int, rank: int):
+    """(first, count): the contiguous range of the `units` (b, h) slices that
+    rank `rank` of `world` takes (attn_shard_range of the C ABI)."""
+    first, count = ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = load_library().attn_shard_range(int(units), int(world), int(rank), ctypes.byref(first),
+                                         ctypes.byref(count))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_shard_range")
+    return first.value, count.value
+
+
+def attn_fwd_sharded(q, k, v, scale=None, causal=True, rank=None, world=None, device=None,
+                     stream=None):
+    """This rank's share of one forward split over processes, one per GPU.
+
+    q, k, v: the whole problem's contiguous [B, H, S, D] bf16/fp16 tensors, on
+    the host or on this rank's GPU.  rank / world default to the
+    torch.distributed process group's.  The rank takes the slices
+    shard_range(B·H, world, rank) gives it, moves only those to `device`
+    (default: the current CUDA device) and runs attn_fwd on them as one
+    [1, count, S, D] problem.  Nothing is exchanged between ranks.  Returns
+    (first, count, out [count, S, D], lse [count, S]) on `device`; count may be
+    0 (then out and lse are empty).
+    """
+    if rank is None or world is None:
+        import torch.distributed as dist
+        rank = dist.get_rank() if rank is None else rank
+        world = dist.get_world_size() if world is None else world
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, S, D] tensor")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v must share a shape")
+    B, H, S, D = q.shape
+    first, count = shard_range(B * H, world, rank)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if count == 0:
+        return first, 0, torch.empty((0, S, D), dtype=q.dtype, device=dev), \
+            torch.empty((0, S), dtype=torch.float32, device=dev)
+    part = [t.view(B * H, S, D)[first:first + count].to(dev).unsqueeze(0) for t in (q, k, v)]
+    out, lse = attn_fwd(*part, scale=scale, causal=causal, stream=stream)
+    return first, count, out[0], lse[0]
 
 
 class _AttentionFn(torch.autograd.Function):

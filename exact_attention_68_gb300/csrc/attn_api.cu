@@ -316,6 +316,16 @@ const char* attn_status_string(attn_status_t status) {
   return "unknown status";
 }
 
+attn_status_t attn_shard_range(int64_t units, int world, int rank, int64_t* first,
+                               int64_t* count) {
+  if (units < 0 || world < 1 || rank < 0 || rank >= world || !first || !count)
+    return ATTN_ERR_INVALID_ARG;
+  const int64_t base = units / world, extra = units % world;
+  *count = base + (rank < extra ? 1 : 0);
+  *first = rank * base + (rank < extra ? rank : extra);
+  return ATTN_OK;
+}
+
 int attn_abi_version(void) { return 1; }
 
 int attn_last_cuda_error(void) { return ea::g_last_cuda_error; }

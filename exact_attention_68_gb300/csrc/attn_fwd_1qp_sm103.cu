@@ -25,6 +25,10 @@
 // schedule's order and an SM that finishes early takes more of them, as with
 // a grid of one CTA per tile, without a counter in global memory.
 //
+// L2: K and V are loaded with an evict-last policy, Q rows and the output,
+// each touched once, with evict-first, so that the heads in flight keep their
+// K/V in L2 (the grid order of schedule.h groups heads for that).
+//
 // Layout (D = 128; D = 64 halves the tiles): K and V rings of 128-row tiles
 // (3 + 3 stages of 32 KB), a 32 KB staging buffer for the output, and a ring
 // of four tile slots that the producer fills.  TMEM columns: S buffers
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
     for (int u = 0; u < D / 8; ++u) {
       const int col = 8 * u;
       const uint4 x = valid && col < p.d_cols && dbg_row(dbb, bh0, grow, col, 8, kChkPQLoad)
-                          ? __ldg(reinterpret_cast<const uint4*>(qr + col))
+                          ? ldg_policy(qr + col, l2_policy_evict_first())
                           : make_uint4(0u, 0u, 0u, 0u);
       qw[4 * u] = x.x, qw[4 * u + 1] = x.y, qw[4 * u + 2] = x.z, qw[4 * u + 3] = x.w;
     }
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
           for (int u = 0; u < 8; ++u) {
             const int col = 64 * c + 8 * u;
             const uint4 xq = nvalid && col < p.d_cols && dbg_row(dbb, nbh, ngrow, col, 8, kChkPQLoad)
-                                 ? __ldg(reinterpret_cast<const uint4*>(qr + col))
+                                 ? ldg_policy(qr + col, l2_policy_evict_first())
                                  : make_uint4(0u, 0u, 0u, 0u);
             w[4 * u] = xq.x, w[4 * u + 1] = xq.y, w[4 * u + 2] = xq.z, w[4 * u + 3] = xq.w;
           }
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
         for (int c = 0; c < D / 64; ++c) {
           const uint32_t src = sb + L::kStageOff + c * kChunkBytes + warp * 32 * 128;
           if (64 * c < p.d_cols && dbg_tma(dbb, src, 32 * 128, c * 64, y0, bh, true, kChkPStore))
-            tma_store_3d(&p.tm_o, src, c * 64, y0, bh);
+            tma_store_3d_policy(&p.tm_o, src, c * 64, y0, bh, l2_policy_evict_first());
         }
         tma_store_commit();
       }

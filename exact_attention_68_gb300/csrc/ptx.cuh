@@ -269,6 +269,25 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
+// 16-byte read-only global load with an L2 cache policy (createpolicy).
+__device__ __forceinline__ uint4 ldg_policy(const void* ptr, uint64_t policy) {
+  uint4 r;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(ptr), "l"(policy));
+  return r;
+}
+
+// 3-D tiled store shared → global with an L2 cache policy.
+__device__ __forceinline__ void tma_store_3d_policy(const CUtensorMap* map, uint32_t src, int x,
+                                                    int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
 // Brings one box of a tiled tensor into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"

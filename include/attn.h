@@ -248,6 +248,35 @@ ATTN_API attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, 
                                    int64_t D, float scale, int causal, attn_dtype_t dtype,
                                    uint64_t wait_timeout_ns, cudaStream_t stream);
 
+/*
+ * attn_shard_range — the (batch, head) slices that rank `rank` of `world`
+ * processes takes when one forward is split over several GPUs, one process
+ * per GPU.
+ *
+ * The FlashAttention-2 blog ("FlashAttention-2 Optimizations" §3) parallelises
+ * the forward over batch and heads (and the sequence); every (b, h) slice is
+ * computed from its own q, k, v rows alone, so a split over processes needs no
+ * exchange of data between them.  Slices are numbered b·H + h (the order of
+ * the [B, H, S, D] layout); rank r takes the contiguous range
+ * [*first, *first + *count), the first (units mod world) ranks one slice more
+ * than the others, so the ranges of ranks 0 .. world-1 cover 0 .. units-1
+ * once, in order.  A rank's slices of a contiguous [B, H, S, D] tensor are
+ * themselves a contiguous [count, S, D] tensor starting at element
+ * first·S·D: attn_fwd with B = 1, H = count on pointers offset that
+ * far computes exactly those slices.  A rank may get no slice (count 0) when
+ * world > units.
+ *
+ *   units        number of slices, B·H (>= 0)
+ *   world, rank  number of processes (>= 1) and this process's index in [0, world)
+ *   first, count outputs (host pointers)
+ *
+ * Host-only arithmetic: no CUDA call, no allocation.  Returns
+ * ATTN_ERR_INVALID_ARG (outputs untouched) for units < 0, world < 1, rank
+ * outside [0, world) or a NULL output pointer.
+ */
+ATTN_API attn_status_t attn_shard_range(int64_t units, int world, int rank, int64_t* first,
+                                        int64_t* count);
+
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status_t status);
 
