@@ -50,8 +50,8 @@ KERNEL_SOURCES = ["exact_attention_68_gb300/csrc/attn_fwd_1qp_sm103.cu",
 # were taken on (a changed kernel reports null until captured again).
 NCU_TRAFFIC_BYTES = {
     # B=1 H=32 S=16384 D=128 causal (attn_fwd_1qp_kernel<128,true,bf16>):
-    # 601,260,800 read + 117,115,648 written
-    "6c260678af76fa23": 718376448,
+    # 570,151,936 read + 112,460,032 written
+    "5457abe89aeedc78": 682611968,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -213,7 +213,9 @@ def bench_config(w, world, scale):
     return {"workload": w.about, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
             "global_batch": w.B * world, "scale": scale,
             "seed": "rank r holds batch block r, drawn with seed r (rank 0: seed 0)",
-            "l2": "inputs 403 MB > 129 MB L2: no flush between steps",
+            "l2": (f"inputs {3 * w.B * w.H * w.S * w.D * 2 / 1e6:.0f} MB "
+                   f"{'>' if 3 * w.B * w.H * w.S * w.D * 2 > 129e6 else '<='} 129 MB L2: "
+                   "no flush between steps"),
             "parallelism": f"head-sharded x{world}: the global problem's (b, h) slices split "
                            "contiguously over the ranks (attn_shard_range), no collective"}
 
@@ -222,7 +224,7 @@ def run_reference(args, world, rank):
     """The oracle on the host cores: `steps` timed samples after `warmup` untimed ones."""
     if rank != 0:
         return
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     qn, kn, vn = as_numpy(*make_qkv(w, seed=0))
     scale = default_scale(w.D)
     rows_per_step = 256  # the same per-head sample as the cpu_baseline leg of the other arm
@@ -427,7 +429,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     build_library()
     binding.load_library()
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     if args.shape:
         B, H, S, D = (int(x) for x in args.shape.split(","))
         w = Workload("shape", B, H, S, D, True, about=f"causal B={B} H={H} S={S} D={D}, N(0,1)")
@@ -471,15 +473,17 @@ def run_ours(args, world, rank, local):
     # clock check: the same step back to back for about a second (not part of
     # the value), long enough for several clock samples; its per-launch time
     # times the median SM clock gives the cycles a launch takes
-    n_chk = max(10, int(1000.0 / max(ms / args.steps, 1e-3)))
-    c0 = time.time()
-    chk_ms = time_steps(step, n_chk, stream) / n_chk
-    c1 = time.time()
-    chk = clocks.summary(c0, c1)
-    clock_check = {"launches": n_chk, "ms_per_launch": chk_ms, "sm_mhz_median": chk["sm_mhz"],
-                   "reasons": chk["reasons"], "samples": chk["samples"],
-                   "mcycles_per_launch": (chk_ms * 1e-3 * chk["sm_mhz"] * 1e6 / 1e6
-                                          if chk["sm_mhz"] else None)}
+    clock_check = None
+    if args.clock_check_s > 0:
+        n_chk = max(10, int(args.clock_check_s * 1000.0 / max(ms / args.steps, 1e-3)))
+        c0 = time.time()
+        chk_ms = time_steps(step, n_chk, stream) / n_chk
+        c1 = time.time()
+        chk = clocks.summary(c0, c1)
+        clock_check = {"launches": n_chk, "ms_per_launch": chk_ms, "sm_mhz_median": chk["sm_mhz"],
+                       "reasons": chk["reasons"], "samples": chk["samples"],
+                       "mcycles_per_launch": (chk_ms * 1e-3 * chk["sm_mhz"]
+                                              if chk["sm_mhz"] else None)}
 
     # end to end: host inputs (pinned) -> device -> kernel -> host outputs, per step
     out_h = torch.empty_like(q_h).pin_memory()
@@ -574,6 +578,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time")
     ap.add_argument("--shape", default=None,
                     help="B,H,S,D of a causal workload to time instead (profiling runs)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOADS),
+                    help="which workload the timed steps run (profiling runs; default c5)")
+    ap.add_argument("--clock-check-s", type=float, default=1.0,
+                    help="seconds of back-to-back steps after the timed region whose clocks "
+                         "are sampled (0: none)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
