@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include "schedule.h"
+
 namespace ea {
 
 // Both backward kernels: warps 0-7 elementwise (two groups of four warps, one
@@ -33,6 +35,9 @@ struct BwdParams {
   int d_cols;            // the tensors' head dimension (<= the kernel's D, a multiple
                          // of 8); the kernel's columns past it are zero
   int n_t;               // ceil(S / 128): tiles along the sequence
+  UnitSchedule sched;    // CTA index -> (b·H + h, unit level): the level of a Q tile i
+                         // is i, of a K/V tile j is n_t - 1 - j (both cost level + 1
+                         // tile-steps under the causal mask)
   float scale;           // softmax scale
   float scale_log2;      // scale · log2(e)
   uint64_t timeout_ns;

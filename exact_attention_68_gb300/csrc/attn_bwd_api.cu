@@ -86,6 +86,13 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
   p.d_cols = static_cast<int>(D);
   p.n_t = static_cast<int>((S + 127) / 128);
   if (static_cast<int64_t>(p.BH) * p.n_t > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de == cudaSuccess) de = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (de != cudaSuccess) return ea::cuda_failure(static_cast<int>(de));
+  // one grid order for both kernels: each streams one slice's tiles of two
+  // tensors (K, V or Q, dout), as many bytes as the forward's K, V
+  p.sched = ea::plan_schedule(BH, p.n_t, S, D, causal != 0, ea::kL2GroupBytes, sms);
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = wait_timeout_ns;

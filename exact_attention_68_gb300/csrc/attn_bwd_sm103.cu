@@ -186,12 +186,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Q tile i of slice bh; the tiles with the most K/V tiles first
+  // Q tile i of slice bh, in the order of the grid schedule (schedule.h):
+  // heavy tiles by L2-sized groups of heads, then the light ones over all heads
   const DbgBounds dbb{p.status, sb, smem_u32(smem_raw) + static_cast<uint32_t>(L::kAlloc), p.S,
                       p.d_cols, p.BH};
-  const int level = blockIdx.x / p.BH;
-  const int bh = blockIdx.x - level * p.BH;
-  const int i = p.n_t - 1 - level;
+  int bh, i;
+  schedule_unit(p.sched, static_cast<int>(blockIdx.x), &bh, &i);
   const int nkv = CAUSAL ? i + 1 : p.n_t;
 
   if (threadIdx.x == 0) {
@@ -560,11 +560,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
   const int lane = threadIdx.x & 31;
 
   // K/V tile j of slice bh; under the mask tile j meets Q tiles j .. n_t-1,
-  // so ascending j is heaviest first
+  // so its schedule level is n_t - 1 - j (grid order as in the dq kernel)
   const DbgBounds dbb{p.status, sb, smem_u32(smem_raw) + static_cast<uint32_t>(L::kAlloc), p.S,
                       p.d_cols, p.BH};
-  const int j = blockIdx.x / p.BH;
-  const int bh = blockIdx.x - j * p.BH;
+  int bh, level;
+  schedule_unit(p.sched, static_cast<int>(blockIdx.x), &bh, &level);
+  const int j = p.n_t - 1 - level;
   const int i0 = CAUSAL ? j : 0;
   const int nq = p.n_t - i0;
   const int n_sub = 4 * nq;  // quarter sub-steps
