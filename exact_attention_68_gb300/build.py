@@ -39,7 +39,7 @@ def _nvcc() -> str:
 
 def _sources():
     return [os.path.join(CSRC, f) for f in ("attn_api.cu", "attn_fwd_1q_sm103.cu", "attn_fwd_1qp_sm103.cu",
-                                            "attn_noalloc.cu", "attn_bwd_api.cu", "attn_bwd_sm103.cu")]
+                                            "attn_noalloc.cu", "attn_bwd_api.cu", "attn_bwd_sm103.cu", "attn_bwd256_sm103.cu")]
 
 
 def _deps():

@@ -23,6 +23,12 @@ struct BwdParams {
   CUtensorMap tm_dq;  // dq, box 64 x 32 rows (one warp's rows)
   CUtensorMap tm_dk;  // dk, same
   CUtensorMap tm_dv;  // dv, same
+  // 256-column kernels only (head dimension above 128): boxes of 64 columns x
+  // 64 rows, for the 64-key (K, V) and 64-query (Q, dout) steps
+  CUtensorMap tm_q64;
+  CUtensorMap tm_k64;
+  CUtensorMap tm_v64;
+  CUtensorMap tm_do64;
   const uint16_t* q;     // 16-bit [B·H, S, d_cols]: rows read into TMEM by the dq kernel
   const uint16_t* k;     // 16-bit [B·H, S, d_cols]: rows read into TMEM by the dk/dv kernel
   const uint16_t* v;     // 16-bit [B·H, S, d_cols]: rows read into TMEM by the dk/dv kernel
@@ -46,5 +52,10 @@ struct BwdParams {
 // Launches the dq kernel (which also writes delta) and then the dk/dv kernel
 // on `stream`.  f16: the 16-bit tensors are fp16 (else bf16).
 cudaError_t bwd_launch(const BwdParams& p, int D, bool causal, bool f16, cudaStream_t stream);
+
+// The same for head dimensions above 128 (kernels 256 columns wide): the dq
+// kernel, then the dk/dv kernel with one CTA per K/V tile and half of the
+// head dimension.
+cudaError_t bwd256_launch(const BwdParams& p, bool causal, bool f16, cudaStream_t stream);
 
 }  // namespace ea

@@ -24,7 +24,6 @@ attn_status_t validate_bwd(const void* q, const void* k, const void* v, const vo
   // shapes, scale, mask flag, q/k/v/out/lse pointers and alignment
   attn_status_t s = ea::validate_args(q, k, v, out, lse, B, H, S, D, scale, causal);
   if (s != ATTN_OK) return s;
-  if (D > 128) return ATTN_ERR_UNSUPPORTED;  // the backward: D <= 128
   if (!dout || !dq || !dk || !dv || !delta) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u)
@@ -73,6 +72,12 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
       !ea::encode_bhsd_16bit(&p.tm_dk, dk, BH, S, D, 32, f16) ||
       !ea::encode_bhsd_16bit(&p.tm_dv, dv, BH, S, D, 32, f16))
     return ea::cuda_failure(ea::kErrTensorMap);
+  const int width = ea::kernel_head_dim(D);
+  if (width == 256 && (!ea::encode_bhsd_16bit(&p.tm_q64, q, BH, S, D, 64, f16) ||
+                    !ea::encode_bhsd_16bit(&p.tm_k64, k, BH, S, D, 64, f16) ||
+                    !ea::encode_bhsd_16bit(&p.tm_v64, v, BH, S, D, 64, f16) ||
+                    !ea::encode_bhsd_16bit(&p.tm_do64, dout, BH, S, D, 64, f16)))
+    return ea::cuda_failure(ea::kErrTensorMap);
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);
   p.v = static_cast<const uint16_t*>(v);
@@ -96,9 +101,10 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = wait_timeout_ns;
-  // kernels of 64 or 128 columns; the tensor maps carry the real column
+  // kernels of 64, 128 or 256 columns; the tensor maps carry the real column
   // count (zeros read past it, those columns never stored)
-  const cudaError_t e = ea::bwd_launch(p, ea::kernel_head_dim(D), causal != 0, f16, stream);
+  const cudaError_t e = width == 256 ? ea::bwd256_launch(p, causal != 0, f16, stream)
+                                     : ea::bwd_launch(p, width, causal != 0, f16, stream);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return ea::cuda_failure(static_cast<int>(e));

@@ -139,8 +139,8 @@ def _bwd(lib, q=A, k=A + T, v=A + 2 * T, out=A + 3 * T, lse=A + 4 * T, dout=A + 
     (dict(delta=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(S=0), binding.ATTN_ERR_INVALID_ARG),
     (dict(D=100), binding.ATTN_ERR_UNSUPPORTED),
-    (dict(D=136), binding.ATTN_ERR_UNSUPPORTED),   # the forward goes to 256, the backward to 128
-    (dict(D=256), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(D=264), binding.ATTN_ERR_UNSUPPORTED),   # above 256
+    (dict(D=260), binding.ATTN_ERR_UNSUPPORTED),
     (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
     (dict(causal=3), binding.ATTN_ERR_INVALID_ARG),
     (dict(dout=A + 5 * T + 8), binding.ATTN_ERR_MISALIGNED),

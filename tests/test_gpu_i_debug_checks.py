@@ -60,7 +60,8 @@ def test_debug_forward_no_check_fails(dbg, D, bhs, causal, dtype):
 
 
 @pytest.mark.parametrize("D,bhs", [(64, (1, 2, 1)), (64, (2, 1, 300)), (128, (1, 2, 129)),
-                                   (128, (1, 1, 513)), (40, (1, 2, 200)), (96, (2, 1, 257))],
+                                   (128, (1, 1, 513)), (40, (1, 2, 200)), (96, (2, 1, 257)),
+                                   (256, (1, 2, 129)), (136, (2, 1, 200))],
                          ids=lambda x: str(x))
 @pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
 def test_debug_backward_no_check_fails(dbg, D, bhs, causal):
