@@ -421,6 +421,31 @@ def backward_leg(w, q, k, v, out, lse, scale, stream, steps):
             "gpu_launches": 2 * steps}
 
 
+def backward_side(device, stream):
+    """TFLOP/s of the backward at head dimension 256 (its own kernels) on the
+    long-context shape: counted 2.5x the forward's causal FLOPs."""
+    from exact_attention_68_gb300 import binding
+    B, H, S, D = 1, 16, 16384, 256
+    gen = torch.Generator(device=device).manual_seed(D)
+    q, k, v, dout = (torch.randn((B, H, S, D), generator=gen, device=device).to(torch.bfloat16)
+                     for _ in range(4))
+    scale = default_scale(D)
+    out, lse = binding.attn_fwd(q, k, v, scale, True)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    delta = torch.empty_like(lse)
+
+    def call():
+        binding.attn_bwd(q, k, v, out, lse, dout, scale, True, dq, dk, dv, delta)
+
+    for _ in range(3):
+        call()
+    ms = time_steps(call, 5, stream) / 5
+    counted = 2.5 * counted_flops(B, H, S, D, True)
+    return {"d256": {"about": f"causal B={B} H={H} S={S} D={D}, N(0,1)", "ms": ms,
+                     "tflops": counted / (ms * 1e-3) / 1e12,
+                     "kernels": ["attn_bwd_dq256_kernel<true>", "attn_bwd_dkdv256_kernel<true>"]}}
+
+
 def run_ours(args, world, rank, local):
     from exact_attention_68_gb300 import binding
     from exact_attention_68_gb300.build import build_library
@@ -515,6 +540,8 @@ def run_ours(args, world, rank, local):
                            "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
                            "frac": bwd["value"] / float(peaks["bf16_tflops"])}
         extra["backward"] = bwd
+        if rank == 0 and world == 1 and not args.no_side:
+            extra["backward_other"] = backward_side(device, stream)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         checked = []

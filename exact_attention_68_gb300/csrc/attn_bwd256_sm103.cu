@@ -372,14 +372,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq256_kernel(const __
 }
 
 // ============================================================== dk/dv kernel
+//
+// 64-query steps, one Sᵀ/dPᵀ buffer.  D = 256 (the width the library runs
+// on it): one CTA per half of the head dimension, V in shared memory (dPᵀ
+// from two shared-memory operands).  The layout also holds D = 64 and 128
+// (one CTA per K/V tile, K and V both in TMEM, at D = 128 filling the 512
+// columns exactly); there the kernel of attn_bwd_sm103.cu, whose two
+// warpgroups' elementwise work overlaps the tensor core's, is faster.
 
-struct Kv256Layout {
-  static constexpr int kStages = 2;  // Q / dO ring
-  static constexpr int kStatBytes = kStepW * 8;  // (lse·log2e, delta) per query
-  static constexpr int kVOff = 0;
-  static constexpr int kQOff = kVOff + kTile128;
-  static constexpr int kDoOff = kQOff + kStages * kTile64;
-  static constexpr int kStatOff = kDoOff + kStages * kTile64;
+template <int D>
+struct KvQ64Layout {
+  static constexpr bool kSplit = D > 128;            // a CTA per half of the head dimension
+  static constexpr int kCols = kSplit ? 128 : D;     // gradient columns per CTA
+  static constexpr int kChunks = D / 64;             // 64-column blocks of a row
+  static constexpr int kTileQ = kChunks * kBlk64;    // 64 queries x D
+  static constexpr int kStages = kSplit ? 2 : (D == 128 ? 4 : 6);  // Q / dO ring
+  static constexpr int kStatBytes = kStepW * 8;      // (lse·log2e, delta) per query
+  static constexpr int kVOff = 0;                    // V tile (split only)
+  static constexpr int kQOff = kVOff + (kSplit ? kChunks * kBlk128 : 0);
+  static constexpr int kDoOff = kQOff + kStages * kTileQ;
+  static constexpr int kStatOff = kDoOff + kStages * kTileQ;
   static constexpr int kBarOff = kStatOff + kStages * kStatBytes;
   static constexpr int kVFull = 0, kKTmem = 1, kFull = 2, kEmpty = kFull + kStages,
                        kSFull = kEmpty + kStages, kPFull = kSFull + 1, kOFull = kPFull + 1,
@@ -387,14 +399,32 @@ struct Kv256Layout {
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kAlloc = kMiscOff + 16 + 1024;
   static_assert(kAlloc <= 232448, "shared memory budget exceeded");
-  static_assert(2 * kStages * kTile64 >= 2 * 2 * kBlk128, "dK/dV staging must fit the Q/dO ring");
-  static constexpr uint32_t kTmemCols = 512, kSCol = 0, kPCol = 64, kKCol = 128, kDvCol = 256,
-                            kDkCol = 384;
+  // the epilogue stages dV (warpgroup 0) and dK (warpgroup 1), 128 rows x kCols each
+  static_assert(2 * kStages * kTileQ >= 2 * (kCols / 64) * kBlk128, "staging must fit the ring");
+  static constexpr uint32_t kTmemCols = 512, kSCol = 0, kPCol = 64, kKCol = 128,
+                            kVCol = 128 + D / 2, kDvCol = 256, kDkCol = 256 + kCols;
+  static_assert(kSplit || kVCol + D / 2 <= kDvCol, "TMEM budget exceeded");
+  static_assert(kDkCol + kCols <= kTmemCols, "TMEM budget exceeded");
 };
 
-template <bool CAUSAL, bool F16>
-__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const __grid_constant__ BwdParams p) {
-  using L = Kv256Layout;
+// One thread's `n` 32-bit words (n = 16, 32 or 64) into TMEM at `taddr`.
+template <int N>
+__device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&w)[N]) {
+  if constexpr (N == 16) {
+    tmem_st_32x32b_x16(taddr, w);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N / 32; ++c)
+      tmem_st_32x32b_x32(taddr + 32 * c, *reinterpret_cast<const uint32_t(*)[32]>(&w[32 * c]));
+  }
+}
+
+template <int D, bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_q64_kernel(const __grid_constant__ BwdParams p) {
+  using L = KvQ64Layout<D>;
+  constexpr bool kSplit = L::kSplit;
+  constexpr int kCols = L::kCols;
+  constexpr int kTileQ = L::kTileQ;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sb = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint8_t* smem_gen = smem_raw + (sb - smem_u32(smem_raw));  // same window, generic
@@ -405,10 +435,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
   const int lane = threadIdx.x & 31;
   const DbgBounds dbb{p.status, sb, smem_u32(smem_raw) + static_cast<uint32_t>(L::kAlloc), p.S,
                       p.d_cols, p.BH};
-  // the two halves of the head dimension of one K/V tile are neighbouring CTAs
-  const int half = static_cast<int>(blockIdx.x & 1u);
+  // with the head dimension split, the two halves of one K/V tile are neighbouring CTAs
+  const int half = kSplit ? static_cast<int>(blockIdx.x & 1u) : 0;
   int bh, level;
-  schedule_unit(p.sched, static_cast<int>(blockIdx.x >> 1), &bh, &level);
+  schedule_unit(p.sched, static_cast<int>(kSplit ? blockIdx.x >> 1 : blockIdx.x), &bh, &level);
   const int j = p.n_t - 1 - level;  // K/V tile
   const int n_q64 = (p.S + kStepW - 1) / kStepW;
   const int u0 = CAUSAL ? 2 * j : 0;  // first 64-query tile that sees this K/V tile
@@ -439,7 +469,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
   const WaitCtl ctl{abort_addr, p.status, p.timeout_ns};
 
   if (warp < 8) {
-    // ======================= elementwise: K to TMEM, Pᵀ, dSᵀ, epilogue =======================
+    // ======================= elementwise: K (and V) to TMEM, Pᵀ, dSᵀ, epilogue =======================
     const int g = warp >> 2;            // query columns [32g, 32g+32) of every step
     const int wq = warp & 3;
     const int r = wq * 32 + lane;       // key row within the tile (TMEM lane)
@@ -447,23 +477,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
     {
-      // this row's half g of K into TMEM (rows past the end and columns past d_cols: 0)
-      uint32_t kw[64];
+      // this row's half g of K (and of V unless it is in shared memory) into
+      // TMEM; rows past the end and columns past d_cols hold zero
+      constexpr int kU = D / 16;  // 16-byte groups in half a row
+      uint32_t kw[4 * kU], vw[4 * kU];
       const bool in_row = gk < p.S;
-      const int64_t base = ((int64_t)bh * p.S + (in_row ? gk : 0)) * p.d_cols + g * 128;
-      const int lim = p.d_cols - g * 128;
+      const int64_t base = ((int64_t)bh * p.S + (in_row ? gk : 0)) * p.d_cols + g * (D / 2);
+      const int lim = p.d_cols - g * (D / 2);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
+      for (int u = 0; u < kU; ++u) {
         const bool in = in_row && 8 * u < lim &&
-                        dbg_row(dbb, bh, gk, g * 128 + 8 * u, 8, kChkWRowLoad);
-        const uint4 kv = in ? __ldg(reinterpret_cast<const uint4*>(p.k + base) + u)
-                            : make_uint4(0u, 0u, 0u, 0u);
+                        dbg_row(dbb, bh, gk, g * (D / 2) + 8 * u, 8, kChkWRowLoad);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 kv = in ? __ldg(reinterpret_cast<const uint4*>(p.k + base) + u) : z;
         kw[4 * u] = kv.x, kw[4 * u + 1] = kv.y, kw[4 * u + 2] = kv.z, kw[4 * u + 3] = kv.w;
+        if constexpr (!kSplit) {
+          const uint4 vv = in ? __ldg(reinterpret_cast<const uint4*>(p.v + base) + u) : z;
+          vw[4 * u] = vv.x, vw[4 * u + 1] = vv.y, vw[4 * u + 2] = vv.z, vw[4 * u + 3] = vv.w;
+        }
       }
-      const uint32_t tk = tmem_base + lane_bits + L::kKCol + 64 * g;
-      if (dbg_warp(dbg_tmem(dbb, tk, 64, warp, kChkWRowTmem))) {
-        tmem_st_32x32b_x32(tk, *reinterpret_cast<const uint32_t(*)[32]>(&kw[0]));
-        tmem_st_32x32b_x32(tk + 32, *reinterpret_cast<const uint32_t(*)[32]>(&kw[32]));
+      const uint32_t tk = tmem_base + lane_bits + L::kKCol + (D / 4) * g;
+      const uint32_t tv = tmem_base + lane_bits + L::kVCol + (D / 4) * g;
+      if (dbg_warp(dbg_tmem(dbb, tk, D / 4, warp, kChkWRowTmem) &&
+                   (kSplit || dbg_tmem(dbb, tv, D / 4, warp, kChkWRowTmem)))) {
+        tmem_st_row<4 * kU>(tk, kw);
+        if constexpr (!kSplit) tmem_st_row<4 * kU>(tv, vw);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -520,19 +558,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
       mbar_arrive(bar(L::kPFull));
     }
 
-    // ---- epilogue: warpgroup 0 stores dV, 1 stores dK · scale (columns
-    // [128·half, 128·half + 128)), staged in the Q / dO ring (idle once every
-    // MMA has completed)
+    // ---- epilogue: warpgroup 0 stores dV, 1 stores dK · scale (this CTA's
+    // columns), staged in the Q / dO ring (idle once every MMA has completed)
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::kOFull), 0, ctl, kSiteW3ElemO));
     if (ok) {
       tc_fence_after_sync();
       const uint32_t tAcc = tmem_base + lane_bits + (g == 0 ? L::kDvCol : L::kDkCol);
-      const uint32_t stage = sb + L::kQOff + g * 2 * kBlk128;
+      const uint32_t stage = sb + L::kQOff + g * (kCols / 64) * kBlk128;
       const CUtensorMap* map = g == 0 ? &p.tm_dv : &p.tm_dk;
       const float mul = g == 0 ? 1.f : p.scale;
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-        store_chunk<F16>(tAcc + 64 * cc, stage + cc * kBlk128, r, mul, map, 128 * half + 64 * cc,
+      for (int cc = 0; cc < kCols / 64; ++cc)
+        store_chunk<F16>(tAcc + 64 * cc, stage + cc * kBlk128, r, mul, map, kCols * half + 64 * cc,
                          j * kRowsW, bh, wq, lane, dbb);
       if (lane == 0) {
         tma_store_commit();
@@ -541,20 +578,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
     }
     tc_fence_before_sync();
   } else if (warp == 9) {
-    // ======================= producer: V once; Q, dO, stats per 64 queries =======================
+    // ======================= producer: (V once;) Q, dO, stats per 64 queries =======================
     const uint64_t pol = l2_policy_evict_last();
     if (lane == 0) {
-      tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_q64);
       tma_prefetch_desc(&p.tm_do64);
       tma_prefetch_desc(&p.tm_dk);
       tma_prefetch_desc(&p.tm_dv);
-      mbar_arrive_expect_tx(bar(L::kVFull), kTile128);
+      if constexpr (kSplit) {
+        tma_prefetch_desc(&p.tm_v);
+        mbar_arrive_expect_tx(bar(L::kVFull), L::kChunks * kBlk128);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t dst = sb + L::kVOff + c * kBlk128;
-        if (dbg_tma(dbb, dst, kBlk128, c * 64, j * kRowsW, bh, false, kChkWLoadB))
-          tma_load_3d(dst, &p.tm_v, bar(L::kVFull), c * 64, j * kRowsW, bh, pol);
+        for (int c = 0; c < L::kChunks; ++c) {
+          const uint32_t dst = sb + L::kVOff + c * kBlk128;
+          if (dbg_tma(dbb, dst, kBlk128, c * 64, j * kRowsW, bh, false, kChkWLoadB))
+            tma_load_3d(dst, &p.tm_v, bar(L::kVFull), c * 64, j * kRowsW, bh, pol);
+        }
       }
     }
     const int64_t row0 = (int64_t)bh * p.S;
@@ -578,13 +617,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
       }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(L::kFull + st), 2 * kTile64);
+        mbar_arrive_expect_tx(bar(L::kFull + st), 2 * kTileQ);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < L::kChunks; ++c) {
           // a skipped copy leaves the stage's transaction count short: the
           // consumer's bounded wait then ends the kernel
-          const uint32_t qd = sb + L::kQOff + st * kTile64 + c * kBlk64;
-          const uint32_t dd = sb + L::kDoOff + st * kTile64 + c * kBlk64;
+          const uint32_t qd = sb + L::kQOff + st * kTileQ + c * kBlk64;
+          const uint32_t dd = sb + L::kDoOff + st * kTileQ + c * kBlk64;
           if (dbg_tma(dbb, qd, kBlk64, c * 64, u * kStepW, bh, false, kChkWLoadA))
             tma_load_3d(qd, &p.tm_q64, bar(L::kFull + st), c * 64, u * kStepW, bh, pol);
           if (dbg_tma(dbb, dd, kBlk64, c * 64, u * kStepW, bh, false, kChkWLoadB))
@@ -601,7 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
                             kSiteW3Prod | 0xff);
       }
       if (!ok) {
-        wait_drain(bar(L::kVFull), 0, kDrainLimitNsW);
+        if (kSplit) wait_drain(bar(L::kVFull), 0, kDrainLimitNsW);
         for (int t = max(issued - L::kStages, 0); t < issued; ++t)
           wait_drain(bar(L::kFull + t % L::kStages), (t / L::kStages) & 1, kDrainLimitNsW);
       }
@@ -611,35 +650,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
     // ======================= tcgen05 issuer (warp 8) =======================
     const bool leader = elect_one();
     constexpr uint32_t kIdescS = instr_desc_16bit(kRowsW, kStepW, false, false, F16);
-    constexpr uint32_t kIdescG = instr_desc_16bit(kRowsW, 128, false, true, F16);
-    constexpr uint32_t kTileUnits = kTile64 >> 4;
+    constexpr uint32_t kIdescG = instr_desc_16bit(kRowsW, kCols, false, true, F16);
+    constexpr uint32_t kTileUnits = kTileQ >> 4;
     const uint64_t d_v = smem_desc_sw128(sb + L::kVOff, 16, 1024);
     const uint64_t d_q = smem_desc_sw128(sb + L::kQOff, 16, 1024);
     const uint64_t d_do = smem_desc_sw128(sb + L::kDoOff, 16, 1024);
-    // this CTA's half of the head dimension: blocks 2·half and 2·half+1
-    const uint64_t d_q_mn = smem_desc_sw128(sb + L::kQOff + 2 * half * kBlk64, kBlk64, 1024);
-    const uint64_t d_do_mn = smem_desc_sw128(sb + L::kDoOff + 2 * half * kBlk64, kBlk64, 1024);
+    // this CTA's gradient columns: blocks kCols/64 · half onwards
+    const uint64_t d_q_mn =
+        smem_desc_sw128(sb + L::kQOff + (kCols / 64) * half * kBlk64, kBlk64, 1024);
+    const uint64_t d_do_mn =
+        smem_desc_sw128(sb + L::kDoOff + (kCols / 64) * half * kBlk64, kBlk64, 1024);
     auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
       return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
     };
     bool ok = wait_warp(bar(L::kKTmem), 0, kSiteW3MmaKV);
-    if (ok) ok = wait_warp(bar(L::kVFull), 0, kSiteW3MmaKV | 1);
+    if (ok && kSplit) ok = wait_warp(bar(L::kVFull), 0, kSiteW3MmaKV | 1);
     for (int t = 0; t < n_sub && ok; ++t) {
       const int st = t % L::kStages;
       ok = wait_warp(bar(L::kFull + st), (t / L::kStages) & 1, kSiteW3MmaQ | (t & 0xff));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader && dbg_smem(dbb, sb + L::kQOff + st * kTile64, kTile64, 1024, kChkWMmaA) &&
-          dbg_smem(dbb, sb + L::kDoOff + st * kTile64, kTile64, 1024, kChkWMmaB)) {
-        // Sᵀ = K · Q_tᵀ (A = K from TMEM) and dPᵀ = V · dO_tᵀ (both from shared memory)
+      if (leader && dbg_smem(dbb, sb + L::kQOff + st * kTileQ, kTileQ, 1024, kChkWMmaA) &&
+          dbg_smem(dbb, sb + L::kDoOff + st * kTileQ, kTileQ, 1024, kChkWMmaB)) {
+        // Sᵀ = K · Q_tᵀ (A = K from TMEM) and dPᵀ = V · dO_tᵀ (A = V from
+        // TMEM, or from shared memory when the head dimension is split)
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
+        for (int kk = 0; kk < D / 16; ++kk)
           mma_ts(tmem_base + L::kSCol, tmem_base + L::kKCol + kk * 8,
                  d_q + st * kTileUnits + kstep_off(kk, kBlk64), kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          mma_ss(tmem_base + L::kPCol, d_v + kstep_off(kk, kBlk128),
-                 d_do + st * kTileUnits + kstep_off(kk, kBlk64), kIdescS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t db = d_do + st * kTileUnits + kstep_off(kk, kBlk64);
+          if constexpr (kSplit)
+            mma_ss(tmem_base + L::kPCol, d_v + kstep_off(kk, kBlk128), db, kIdescS, kk > 0 ? 1u : 0u);
+          else
+            mma_ts(tmem_base + L::kPCol, tmem_base + L::kVCol + kk * 8, db, kIdescS, kk > 0 ? 1u : 0u);
+        }
         mma_commit(bar(L::kSFull));
       }
       __syncwarp();
@@ -647,7 +693,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
       if (!ok) break;
       tc_fence_after_sync();
       if (leader) {
-        // dV += Pᵀ · dO_t and dK += dSᵀ · Q_t over this CTA's 128 columns (16 queries per step)
+        // dV += Pᵀ · dO_t and dK += dSᵀ · Q_t over this CTA's columns (16 queries per step)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
@@ -674,14 +720,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv256_kernel(const 
   }
 }
 
+template <int D, bool CAUSAL, bool F16>
+cudaError_t dkdv_q64_launch(const BwdParams& p, cudaStream_t stream) {
+  using L = KvQ64Layout<D>;
+  auto kkv = attn_bwd_dkdv_q64_kernel<D, CAUSAL, F16>;
+  cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  // with the head dimension split, two CTAs (column halves) per K/V tile
+  cfg.gridDim = dim3(static_cast<unsigned>((L::kSplit ? 2ll : 1ll) * p.BH * p.n_t), 1, 1);
+  cfg.blockDim = dim3(kBwdThreads, 1, 1);
+  cfg.stream = stream;
+  cfg.dynamicSmemBytes = L::kAlloc;
+  return cudaLaunchKernelEx(&cfg, kkv, p);
+}
+
 template <bool CAUSAL, bool F16>
 cudaError_t launch_256(const BwdParams& p, cudaStream_t stream) {
   auto kdq = attn_bwd_dq256_kernel<CAUSAL, F16>;
-  auto kkv = attn_bwd_dkdv256_kernel<CAUSAL, F16>;
   cudaError_t e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Dq256Layout::kAlloc);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, Kv256Layout::kAlloc);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((long long)p.BH * p.n_t), 1, 1);
@@ -690,9 +748,7 @@ cudaError_t launch_256(const BwdParams& p, cudaStream_t stream) {
   cfg.dynamicSmemBytes = Dq256Layout::kAlloc;
   e = cudaLaunchKernelEx(&cfg, kdq, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(static_cast<unsigned>(2ll * p.BH * p.n_t), 1, 1);  // two column halves
-  cfg.dynamicSmemBytes = Kv256Layout::kAlloc;
-  return cudaLaunchKernelEx(&cfg, kkv, p);
+  return dkdv_q64_launch<256, CAUSAL, F16>(p, stream);
 }
 
 }  // namespace

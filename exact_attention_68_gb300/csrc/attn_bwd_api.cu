@@ -74,9 +74,9 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
     return ea::cuda_failure(ea::kErrTensorMap);
   const int width = ea::kernel_head_dim(D);
   if (width == 256 && (!ea::encode_bhsd_16bit(&p.tm_q64, q, BH, S, D, 64, f16) ||
-                    !ea::encode_bhsd_16bit(&p.tm_k64, k, BH, S, D, 64, f16) ||
-                    !ea::encode_bhsd_16bit(&p.tm_v64, v, BH, S, D, 64, f16) ||
-                    !ea::encode_bhsd_16bit(&p.tm_do64, dout, BH, S, D, 64, f16)))
+                       !ea::encode_bhsd_16bit(&p.tm_k64, k, BH, S, D, 64, f16) ||
+                       !ea::encode_bhsd_16bit(&p.tm_v64, v, BH, S, D, 64, f16) ||
+                       !ea::encode_bhsd_16bit(&p.tm_do64, dout, BH, S, D, 64, f16)))
     return ea::cuda_failure(ea::kErrTensorMap);
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);
