@@ -100,18 +100,18 @@ def test_plan_rules(shim, BH, S, D, causal):
         assert tail == 0
     else:
         assert 0 <= tail <= nu
-        want = 2 * nu * sms
+        want = nu * sms // 2
         assert tail == nu or tail * tail * BH >= want
         assert tail == 0 or (tail - 1) ** 2 * BH < want  # the smallest such tail
 
 
 def test_plan_long_context_causal(shim):
     # B=1, H=32, S=16384, D=128: 8 MiB of K/V per slice -> 6 slices per group;
-    # 128 Q tiles, sqrt(2 * 128 * 152 / 32) = 34.9 -> 35 levels in phase 2
-    assert _plan(shim, 32, 128, 16384, 128, True) == (6, 35)
+    # 128 Q tiles, sqrt(128 * 152 / (2 * 32)) = 17.4 -> 18 levels in phase 2
+    assert _plan(shim, 32, 128, 16384, 128, True) == (6, 18)
     # B=2, H=16, S=4096, D=128: 2 MiB per slice -> 24 per group; 32 Q tiles,
-    # sqrt(2 * 32 * 152 / 32) = 17.4 -> 18 tail levels
-    assert _plan(shim, 32, 32, 4096, 128, True) == (24, 18)
+    # sqrt(32 * 152 / (2 * 32)) = 8.7 -> 9 tail levels
+    assert _plan(shim, 32, 32, 4096, 128, True) == (24, 9)
     # without the mask every unit costs the same: no phase 2
     assert _plan(shim, 128, 16, 2048, 128, False) == (48, 0)
 
