@@ -50,8 +50,8 @@ KERNEL_SOURCES = ["exact_attention_68_gb300/csrc/attn_fwd_1qp_sm103.cu",
 # were taken on (a changed kernel reports null until captured again).
 NCU_TRAFFIC_BYTES = {
     # B=1 H=32 S=16384 D=128 causal (attn_fwd_1qp_kernel<128,true,bf16>):
-    # 570,151,936 read + 112,460,032 written
-    "5457abe89aeedc78": 682611968,
+    # 442,098,432 read + 113,681,920 written
+    "30f4549411964bfc": 555780352,
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -314,12 +314,25 @@ def blas_threads():
     return os.cpu_count(), "os.cpu_count (no BLAS thread query available)"
 
 
-def oracle_per_config(budget_s, full_cap_s=30.0):
+def full_parity(ref_out, ref_lse, out, lse):
+    """Every element of a GPU output against the oracle's, with the parity bars."""
+    og, lg = out.double().numpy(), lse.double().numpy()
+    err, lerr = np.abs(og - ref_out), np.abs(lg - ref_lse)
+    res = {"rows": int(lg.size), "out_max_err": float(err.max()),
+           "out_mean_err": float(err.mean()), "lse_max_err": float(lerr.max())}
+    res["pass"] = bool(res["out_max_err"] <= 2e-2 and res["out_mean_err"] <= 2e-3
+                       and res["lse_max_err"] <= 1e-3 and np.isfinite(og).all())
+    return res
+
+
+def oracle_per_config(budget_s, full_cap_s=30.0, kept=None):
     """Wall time of the fp64 oracle on c1-c4.  c1 runs whole.  c2-c4 are first
     timed on evenly spaced rows of every head for about `budget_s` seconds;
     c2 and c4 then run whole if that rate puts the whole problem under
     `full_cap_s`, and c3 (like c5, the cpu_baseline) keeps the time
-    extrapolated from the rate in counted FLOPs, flagged as such."""
+    extrapolated from the rate in counted FLOPs, flagged as such.  With
+    `kept` (the GPU outputs of the side timings), each entry also carries the
+    GPU output's errors against the oracle on the rows it computed."""
     from oracle import attention_fwd
     res = {}
     for name in ("c1", "c2", "c3", "c4"):
@@ -330,23 +343,30 @@ def oracle_per_config(budget_s, full_cap_s=30.0):
         rows = w.B * w.H * w.S
         est = None
         if name != "c1":
+            checked = []
             tf, n_rows, secs = oracle_rows_sample(qn, kn, vn, scale, w.causal, min(w.S, 256),
-                                                  list(range(w.H)), budget_s)
+                                                  list(range(w.H)), budget_s, checked)
             est = total / (tf * 1e12)
             if name == "c3" or est > full_cap_s:
                 res[name] = {"rows": n_rows, "s": secs, "tflops": tf, "full_s": est,
                              "extrapolated": True}
+                if kept is not None and name in kept:
+                    res[name]["parity"] = parity_of_outputs(checked, *kept[name])
                 continue
         t0 = time.perf_counter()
-        attention_fwd(qn, kn, vn, scale, w.causal)
+        ref_out, ref_lse = attention_fwd(qn, kn, vn, scale, w.causal)
         secs = time.perf_counter() - t0
         res[name] = {"rows": rows, "s": secs, "tflops": total / secs / 1e12, "full_s": secs,
                      "extrapolated": False, "sample_estimate_s": est}
+        if kept is not None and name in kept:
+            res[name]["parity"] = full_parity(ref_out, ref_lse, *kept[name])
     return res
 
 
-def side_workloads(device, stream):
-    """TFLOP/s of the other workloads (context; L2 flushed between launches)."""
+def side_workloads(device, stream, kept=None):
+    """TFLOP/s of the other workloads (context; L2 flushed between launches).
+    If `kept` is a dict, c1-c4's last outputs are copied into it (host tensors)
+    for the per-workload parity check of the CPU leg."""
     from exact_attention_68_gb300 import binding
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
     res = {}
@@ -367,6 +387,8 @@ def side_workloads(device, stream):
             e.synchronize()
             times.append(s.elapsed_time(e))
         ms = statistics.median(times)
+        if kept is not None:
+            kept[name] = (out.cpu(), lse.cpu())
         res[name] = {"about": w.about, "ms": ms,
                      "tflops": counted_flops(w.B, w.H, w.S, w.D, w.causal) / (ms * 1e-3) / 1e12}
     # the default workload with fp16 inputs (attn_fwd_ex), 20 back-to-back launches
@@ -443,7 +465,7 @@ def backward_side(device, stream):
     counted = 2.5 * counted_flops(B, H, S, D, True)
     return {"d256": {"about": f"causal B={B} H={H} S={S} D={D}, N(0,1)", "ms": ms,
                      "tflops": counted / (ms * 1e-3) / 1e12,
-                     "kernels": ["attn_bwd_dq256_kernel<true>", "attn_bwd_dkdv256_kernel<true>"]}}
+                     "kernels": ["attn_bwd_dq256_kernel<true>", "attn_bwd_dkdv_q64_kernel<256,true>"]}}
 
 
 def run_ours(args, world, rank, local):
@@ -532,8 +554,9 @@ def run_ours(args, world, rank, local):
     traffic = NCU_TRAFFIC_BYTES.get(kernel_hash())
     value = flops * world * args.steps / (ms_max * 1e-3) / 1e12
     extra = {}
+    kept_outputs = {}
     if rank == 0 and world == 1 and not args.no_side:
-        extra["other_workloads"] = side_workloads(device, stream)
+        extra["other_workloads"] = side_workloads(device, stream, kept_outputs)
     if not args.no_bwd:
         bwd = backward_leg(w, q, k, v, out, lse, scale, stream, max(3, min(args.steps, 50)))
         bwd["roofline"] = {"bound": "tensor", "achieved": bwd["value"],
@@ -555,7 +578,7 @@ def run_ours(args, world, rank, local):
                          f"{w.about} workload, oracle row form in fp64 numpy, {secs:.1f} s"}
         extra["parity"] = parity_of_outputs(checked, out_h, lse_h)
         if not args.no_side:
-            extra["oracle_per_config"] = oracle_per_config(args.cpu_budget / 4)
+            extra["oracle_per_config"] = oracle_per_config(args.cpu_budget / 4, kept=kept_outputs)
     if rank != 0:
         return
     nb = w.B * w.H * w.S * w.D * 2

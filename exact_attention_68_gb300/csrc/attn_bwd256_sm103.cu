@@ -23,7 +23,7 @@
 //       values per column), dQ [256, 512).  dO stays in shared memory (64 KB),
 //       so dP = dO·Vᵀ reads both operands from shared memory; K and V stream
 //       in 64-key tiles (3 + 2 stages of 32 KB).
-//   attn_bwd_dkdv256_kernel one CTA per (b·H + h, 128-row K/V tile, half of the
+//   attn_bwd_dkdv_q64_kernel<256> one CTA per (b·H + h, 128-row K/V tile, half of the
 //       head dimension): dK and dV of 128 columns each.  TMEM: Sᵀ [0, 64),
 //       dPᵀ [64, 128) of one 64-query step, K [128, 256), dV [256, 384),
 //       dK [384, 512).  V stays in shared memory (64 KB); Q and dO stream in
