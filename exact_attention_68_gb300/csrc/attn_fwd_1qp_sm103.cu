@@ -112,7 +112,14 @@ __device__ __forceinline__ int kv_steps(int i, int n_kt) {
   return CAUSAL ? (i + 1 < n_kt ? i + 1 : n_kt) : n_kt;
 }
 
-template <int D, bool CAUSAL, bool F16>
+// QCP selects how a tile's Q rows reach tensor memory.  false: the softmax
+// warps load them (the next tile's while the current one drains) and store
+// them with tcgen05.st.  true: the producer brings them into the K ring with
+// TMA, ahead of the tile's K tiles, and the MMA warp copies them in with
+// tcgen05.cp, so the softmax warps go straight from a tile's last step to its
+// epilogue; that shortens every tile hand-over, and pays off for short tiles
+// (fwd1qp_launch chooses).
+template <int D, bool CAUSAL, bool F16, bool QCP>
 __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid_constant__ Fwd1QParams p) {
   using L = LayoutP<D>;
   constexpr int kTile = L::kTile, kChunkBytes = L::kChunkBytes;
@@ -133,7 +140,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
   // The first tile is this CTA's own.  A softmax thread's row of its Q is
   // requested before the set-up below, so that the load's latency overlaps it.
   uint32_t qw[D / 2];
-  if (warp < 4) {
+  if (!QCP && warp < 4) {
     int bh0, i0;
     schedule_unit(p.sched, static_cast<int>(blockIdx.x), &bh0, &i0);
     const int grow = i0 * kRowsP + warp * 32 + lane;
@@ -149,7 +156,10 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
     }
   }
 
-  if (threadIdx.x == 0) {
+  // With QCP the producer thread sets up the barriers and at once starts the
+  // copy of the first tile's Q rows (K-ring position 0), so that the load's
+  // latency overlaps the rest of the set-up.
+  if (threadIdx.x == (QCP ? 5 * 32 : 0)) {
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(L::kKFull + s), 1);
       mbar_init(bar(L::kKEmpty + s), 1);
@@ -173,6 +183,18 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
     mbar_init(bar(L::kDrain), 1);
     st_volatile_shared(abort_addr, 0);
     fence_barrier_init();
+    if constexpr (QCP) {
+      int bh0, i0;
+      schedule_unit(p.sched, static_cast<int>(blockIdx.x), &bh0, &i0);
+      mbar_arrive_expect_tx(bar(L::kKFull + 0), kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const uint32_t dst = sb + L::kKOff + c * kChunkBytes;
+        if (dbg_tma(dbb, dst, kChunkBytes, c * 64, i0 * kRowsP, bh0, false, kChkPLoadK))
+          tma_load_3d(dst, &p.tm_q, bar(L::kKFull + 0), c * 64, i0 * kRowsP, bh0,
+                      l2_policy_evict_first());
+      }
+    }
   }
   if (warp == 4) {
     tmem_alloc(tmem_slot, L::kTmemCols);
@@ -203,14 +225,16 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
     const uint32_t tO = tmem_base + lane_bits + kOCol;
     const float sl2 = p.scale_log2;
     // Q row of tile 0 into Q slot 0, 32 columns (64 values) per store
+    if constexpr (!QCP) {
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c)
-      if (dbg_warp(dbg_tmem(dbb, tmem_base + lane_bits + kQCol + 32 * c, 32, warp, kChkPQTmem)))
-        tmem_st_32x32b_x32(tmem_base + lane_bits + kQCol + 32 * c,
-                           *reinterpret_cast<const uint32_t(*)[32]>(&qw[32 * c]));
-    tmem_st_wait();
-    tc_fence_before_sync();
-    mbar_arrive(bar(L::kQTmem + 0));
+      for (int c = 0; c < D / 64; ++c)
+        if (dbg_warp(dbg_tmem(dbb, tmem_base + lane_bits + kQCol + 32 * c, 32, warp, kChkPQTmem)))
+          tmem_st_32x32b_x32(tmem_base + lane_bits + kQCol + 32 * c,
+                             *reinterpret_cast<const uint32_t(*)[32]>(&qw[32 * c]));
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kQTmem + 0));
+    }
 
     bool ok = true;
     int x = read_info(0, kSitePSoftInfo, &ok);
@@ -332,12 +356,12 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
       if (!ok) break;
       g += nkv;
 
-      // ---- the next tile: its Q rows into the other Q slot (the producer
-      // brought them into L2), so that its first S products can start while
-      // this tile's output drains
+      // ---- the next tile (without QCP: its Q rows into the other Q slot; the
+      // producer brought them into L2), so that its first S products can
+      // start while this tile's output drains
       const int nx = read_info(k + 1, kSitePSoftInfo, &ok);
       if (!ok) break;
-      if (nx >= 0 && dbg(nx < n_units, dbb, kChkPTile)) {
+      if (!QCP && nx >= 0 && dbg(nx < n_units, dbb, kChkPTile)) {
         int nbh, ni;
         schedule_unit(p.sched, nx, &nbh, &ni);
         const int ngrow = ni * kRowsP + row;
@@ -420,8 +444,11 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
       tma_prefetch_desc(&p.tm_o);
       tma_prefetch_desc(&p.tm_q);
       const uint64_t pol = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
       const uint32_t resp = sb + L::kRespOff;
-      int k_issued = 0, v_issued = 0;  // K / V steps whose loads were issued
+      // K-ring positions / V steps whose loads were issued (with QCP the K ring
+      // also carries each tile's Q rows; tile 0's went out during the set-up)
+      int k_issued = QCP ? 1 : 0, v_issued = 0;
       uint32_t clc_n = 0;   // launch-control requests made
       bool clc_wait = false;  // a request is in flight
       bool ok = true;
@@ -450,11 +477,26 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
         const int nkv = kv_steps<CAUSAL>(i, p.n_kt);
         const int jr = nkv > kAskAhead ? nkv - 1 - kAskAhead : 0;  // ask for the next tile
         int nx = -1;
+        if (QCP && k > 0) {  // the tile's Q rows, ahead of its K tiles
+          const int ks = k_issued % kKStages;
+          ok = wait_bounded(bar(L::kKEmpty + ks), ((k_issued / kKStages) & 1) ^ 1, ctl,
+                            kSitePProdK | (k_issued & 0xff));
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(L::kKFull + ks), kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            const uint32_t dst = sb + L::kKOff + ks * kTile + c * kChunkBytes;
+            if (dbg_tma(dbb, dst, kChunkBytes, c * 64, i * kRowsP, bh, false, kChkPLoadK))
+              tma_load_3d(dst, &p.tm_q, bar(L::kKFull + ks), c * 64, i * kRowsP, bh, pol_q);
+          }
+          ++k_issued;
+        }
         for (int j = 0; j < nkv; ++j) {
           const int gj = g + j;
-          const int ks = gj % kKStages;
-          ok = wait_bounded(bar(L::kKEmpty + ks), ((gj / kKStages) & 1) ^ 1, ctl,
-                            kSitePProdK | (gj & 0xff));
+          const int kp = QCP ? k_issued : gj;  // K-ring position of this K tile
+          const int ks = kp % kKStages;
+          ok = wait_bounded(bar(L::kKEmpty + ks), ((kp / kKStages) & 1) ^ 1, ctl,
+                            kSitePProdK | (kp & 0xff));
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kKFull + ks), kTile);
 #pragma unroll
@@ -465,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
             if (dbg_tma(dbb, dst, kChunkBytes, c * 64, j * kRowsP, bh, false, kChkPLoadK))
               tma_load_3d(dst, &p.tm_k, bar(L::kKFull + ks), c * 64, j * kRowsP, bh, pol);
           }
-          k_issued = gj + 1;
+          k_issued = kp + 1;
           const int vs = gj % kVStages;
           ok = wait_bounded(bar(L::kVEmpty + vs), ((gj / kVStages) & 1) ^ 1, ctl,
                             kSitePProdV | (gj & 0xff));
@@ -481,7 +523,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
           if (j == jr) request();
           if (j == nkv - 1) {
             // settle the next tile: the answer to the request, published for
-            // the other roles; its Q rows are brought into L2
+            // the other roles (without QCP its Q rows are brought into L2)
             if (clc_wait) {
               ok = wait_bounded(bar(L::kClc), (clc_n - 1) & 1, ctl, kSitePClc | (k & 0xff));
               if (!ok) break;
@@ -491,7 +533,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
             }
             ok = publish(k + 1, nx);
             if (!ok) break;
-            if (nx >= 0) {
+            if (!QCP && nx >= 0) {
               int nbh, ni;
               schedule_unit(p.sched, nx, &nbh, &ni);
 #pragma unroll
@@ -532,9 +574,11 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
     auto wait_warp = [&](uint32_t b, uint32_t parity, int site) {
       return __all_sync(0xffffffffu, wait_bounded(b, parity, ctl, site));
     };
-    // S of step gh into buffer gh & 1: Q (slot qs, 8 columns per K step) · K_ghᵀ
-    auto issue_s = [&](int gh, int qs) {
-      const int ks = gh % kKStages;
+    int kpos = 0;  // with QCP: K-ring positions consumed (each tile's Q, then its K tiles)
+    // S of step gh into buffer gh & 1: Q (slot qs, 8 columns per K step) · K_ghᵀ,
+    // K in ring position kp
+    auto issue_s = [&](int gh, int qs, int kp) {
+      const int ks = kp % kKStages;
       if (!dbg_smem(dbb, sb + L::kKOff + ks * kTile, kTile, 1024, kChkPMmaK) ||
           !dbg_tmem_cols(dbb, tmem_base + 128 * (gh & 1), 128, kChkPMmaTmem) ||
           !dbg_tmem_cols(dbb, tmem_base + kQCol + qs * (D / 2), D / 2, kChkPMmaTmem))
@@ -549,16 +593,41 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
       mma_commit(bar(L::kSFull + (gh & 1)));
       mma_commit(bar(L::kKEmpty + ks));
     };
-    // the first (up to) two S products of a tile starting at step g, Q in slot qs
+    // the first (up to) two S products of a tile starting at step g, Q in slot
+    // qs.  With QCP the Q rows are first copied from the K ring into the
+    // slot, which was last read by the S products of tile k - 2: complete by
+    // now, as the P of tile k - 1's last step, which this warp has waited
+    // for, comes after them.
     auto start_tile = [&](int g, int nkv, int qs, int k) {
-      bool r = wait_warp(bar(L::kQTmem + qs), (k >> 1) & 1, kSitePMmaQ | (k & 0xff));
+      bool r;
+      if constexpr (QCP) {
+        const int ks = kpos % kKStages;
+        r = wait_warp(bar(L::kKFull + ks), (kpos / kKStages) & 1, kSitePMmaQ | (k & 0xff));
+        if (!r) return false;
+        tc_fence_after_sync();
+        if (leader && dbg_smem(dbb, sb + L::kKOff + ks * kTile, kTile, 1024, kChkPMmaK) &&
+            dbg_tmem_cols(dbb, tmem_base + kQCol + qs * (D / 2), D / 2, kChkPMmaTmem)) {
+          const uint64_t db = dk + ks * kTileUnits;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tmem_cp_128x256b(tmem_base + kQCol + qs * (D / 2) + kk * 8,
+                             db + (((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4));
+          mma_commit(bar(L::kKEmpty + ks));
+        }
+        __syncwarp();
+        ++kpos;
+      } else {
+        r = wait_warp(bar(L::kQTmem + qs), (k >> 1) & 1, kSitePMmaQ | (k & 0xff));
+      }
       for (int j0 = 0; j0 < 2 && j0 < nkv && r; ++j0) {
         const int gh = g + j0;
-        r = wait_warp(bar(L::kKFull + gh % kKStages), (gh / kKStages) & 1, kSitePMmaK | (gh & 0xff));
+        const int kp = QCP ? kpos : gh;
+        r = wait_warp(bar(L::kKFull + kp % kKStages), (kp / kKStages) & 1, kSitePMmaK | (gh & 0xff));
         if (!r) break;
         tc_fence_after_sync();
-        if (leader) issue_s(gh, qs);
+        if (leader) issue_s(gh, qs, kp);
         __syncwarp();
+        if constexpr (QCP) ++kpos;
       }
       return r;
     };
@@ -596,12 +665,14 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
         }
         __syncwarp();
         if (j + 2 < nkv) {
-          ok = wait_warp(bar(L::kKFull + (gj + 2) % kKStages), ((gj + 2) / kKStages) & 1,
+          const int kp = QCP ? kpos : gj + 2;
+          ok = wait_warp(bar(L::kKFull + kp % kKStages), (kp / kKStages) & 1,
                          kSitePMmaK | ((gj + 2) & 0xff));
           if (!ok) break;
           tc_fence_after_sync();
-          if (leader) issue_s(gj + 2, qs);  // overwrites P_b: P·V of step gj was issued first
+          if (leader) issue_s(gj + 2, qs, kp);  // overwrites P_b: P·V of step gj was issued first
           __syncwarp();
+          if constexpr (QCP) ++kpos;
         }
       }
       if (!ok) break;
@@ -628,9 +699,9 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
   }
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, bool QCP>
 cudaError_t launch_1qp(const Fwd1QParams& p, cudaStream_t stream) {
-  auto kern = attn_fwd_1qp_kernel<D, CAUSAL, F16>;
+  auto kern = attn_fwd_1qp_kernel<D, CAUSAL, F16, QCP>;
   constexpr int kAlloc = LayoutP<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
   if (e != cudaSuccess) return e;
@@ -642,10 +713,24 @@ cudaError_t launch_1qp(const Fwd1QParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int D, bool QCP>
+cudaError_t launch_1qp_q(const Fwd1QParams& p, bool causal, bool f16, cudaStream_t stream) {
+  if (f16)
+    return causal ? launch_1qp<D, true, true, QCP>(p, stream) : launch_1qp<D, false, true, QCP>(p, stream);
+  return causal ? launch_1qp<D, true, false, QCP>(p, stream) : launch_1qp<D, false, false, QCP>(p, stream);
+}
+
+// Q through the K ring and tcgen05.cp (QCP) when a tile meets this many K/V
+// steps on average or fewer: it makes each tile hand-over shorter, which
+// measured 6 % faster on 2x16x4096x128 causal (16.5 steps a tile) and
+// 8x16x2048x128 (16), but 1-2 % slower per step in long tiles.
+constexpr int kQcpMaxAvgSteps = 24;
+
 template <int D>
 cudaError_t launch_1qp_d(const Fwd1QParams& p, bool causal, bool f16, cudaStream_t stream) {
-  if (f16) return causal ? launch_1qp<D, true, true>(p, stream) : launch_1qp<D, false, true>(p, stream);
-  return causal ? launch_1qp<D, true, false>(p, stream) : launch_1qp<D, false, false>(p, stream);
+  const int avg_steps = causal ? (p.n_kt + 1) / 2 : p.n_kt;
+  return avg_steps <= kQcpMaxAvgSteps ? launch_1qp_q<D, true>(p, causal, f16, stream)
+                                      : launch_1qp_q<D, false>(p, causal, f16, stream);
 }
 
 }  // namespace

@@ -407,6 +407,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// TMEM[lanes 0-127, 8 columns from taddr] = a 128-row x 32-byte block of
+// shared memory described by a matrix descriptor (the layout an MMA operand
+// descriptor gives): row r lands in lane r, its 16 16-bit values two per
+// column, which is the A-operand layout of a TS product.  Asynchronous, and
+// executed in order with the tcgen05.mma this thread issues after it.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
