@@ -56,6 +56,32 @@ def test_ragged_head_groups(cuda_device, S, D):
     lg = to_f64(lse)[idx[:, 0], idx[:, 1], idx[:, 2]]
     compare(og, lg, ro, rl, f"ragged groups S={S} D={D}")
 
+# The persistent kernel brings Q into tensor memory one of two ways, chosen by
+# the average K/V steps a tile meets (24 or fewer: through the K ring and
+# tcgen05.cp; more: loaded by the softmax warps).  Shapes on both sides of
+# that line under each mask: causal averages (n_kt + 1) / 2 steps (S = 6144:
+# 24, S = 6272: 25), non-causal n_kt (S = 3072: 24, S = 3200: 25).
+Q_PATH_SHAPES = [(6144, True), (6272, True), (3072, False), (3200, False)]
+
+
+@pytest.mark.parametrize("S,causal", Q_PATH_SHAPES, ids=lambda x: str(x))
+@pytest.mark.parametrize("D", [64, 128])
+def test_both_q_paths(cuda_device, S, causal, D):
+    """Rows 0, 127, 128, S-1 and 256 rows from default_rng(21) of each of the
+    three heads against the oracle."""
+    B, H = 1, 3
+    q, k, v = make_qkv((B, H, S, D), seed=21)
+    scale = default_scale(D)
+    out, lse = run_gpu(q, k, v, scale, causal)
+    rng = np.random.default_rng(21)
+    rows = np.unique(np.concatenate([[0, 127, 128, S - 1], rng.integers(0, S, 256)]))
+    idx = np.asarray([(0, h, int(i)) for h in range(H) for i in rows], dtype=np.int64)
+    ro, rl = _oracle_rows(q, k, v, scale, causal, idx)
+    og = to_f64(out)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    lg = to_f64(lse)[idx[:, 0], idx[:, 1], idx[:, 2]]
+    compare(og, lg, ro, rl, f"S={S} causal={causal} D={D}")
+
+
 EDGE_SHAPES = [
     (1, 1, 1, 64), (1, 1, 1, 128), (1, 1, 7, 64), (1, 1, 7, 128), (2, 3, 129, 64),
     (1, 2, 200, 128), (1, 1, 256, 128), (1, 1, 384, 64), (3, 1, 1000, 128), (1, 2, 640, 64),
