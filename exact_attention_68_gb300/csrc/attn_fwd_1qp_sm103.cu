@@ -647,9 +647,10 @@ __global__ void __launch_bounds__(kThreadsP, 1) attn_fwd_1qp_kernel(const __grid
       for (int j = 0; j < nkv && ok; ++j) {
         const int gj = g + j;
         const int b = gj & 1;
-        ok = wait_warp(bar(L::kPFull + b), (gj >> 1) & 1, kSitePMmaP | (gj & 0xff));
-        if (ok) ok = wait_warp(bar(L::kVFull + gj % kVStages), (gj / kVStages) & 1,
-                               kSitePMmaV | (gj & 0xff));
+        // V of this step has normally landed long before P: waiting for it
+        // first keeps that wait off the path from P to its product
+        ok = wait_warp(bar(L::kVFull + gj % kVStages), (gj / kVStages) & 1, kSitePMmaV | (gj & 0xff));
+        if (ok) ok = wait_warp(bar(L::kPFull + b), (gj >> 1) & 1, kSitePMmaP | (gj & 0xff));
         if (!ok) break;
         tc_fence_after_sync();
         if (leader && dbg_smem(dbb, sb + L::kVOff + (gj % kVStages) * kTile, kTile, 1024, kChkPMmaV) &&
