@@ -393,15 +393,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       const bool more = j + 1 < nkv;
       const int ksn = (j + 1) % L::kKStages;
       const int vsn = (j + 1) % L::kVStages;
-      ok = wait_warp(bar(L::kPFull + 0), j & 1, kSiteDqMmaP | (j & 0x7f));
+      // At D = 64 the next K/V tile is waited for before dS_0 (it has normally
+      // landed long before), which keeps that wait off the path from dS_0 to
+      // S/dP of the next tile; at D = 128 that order measured slower.
+      constexpr bool kKvFirst = D == 64;
+      if (kKvFirst && more) ok = wait_kv(j + 1);
+      if (ok) ok = wait_warp(bar(L::kPFull + 0), j & 1, kSiteDqMmaP | (j & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
       if (leader) issue_g(ks, 0, j == 0);
       __syncwarp();
       if (more) {
-        ok = wait_kv(j + 1);
-        if (!ok) break;
-        tc_fence_after_sync();
+        if (!kKvFirst) {
+          ok = wait_kv(j + 1);
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
         if (leader) issue_sp(ksn, vsn, 0);
         __syncwarp();
       }
@@ -758,18 +765,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
     }
     for (int t = 0; t < n_sub && ok; ++t) {
       const int b = t & 1;
-      ok = wait_warp(bar(L::kPFull + b), (t >> 1) & 1, kSiteKvMmaP | (b << 7) | (t & 0x7f));
-      if (!ok) break;
-      tc_fence_after_sync();
       const int t2 = t + 2;
       if ((t2 & 3) == 0 && t2 < n_sub) {
-        // the next sub-step opens Q tile t2 / 4: its stage must have landed
+        // the sub-step issued after this one opens Q tile t2 / 4: its stage
+        // must have landed (normally long before this P, so waited for first)
         const int it2 = t2 >> 2;
         ok = wait_warp(bar(L::kFull + it2 % L::kStages), (it2 / L::kStages) & 1,
                        kSiteKvMmaQ | (it2 & 0xff));
-        if (!ok) break;
-        tc_fence_after_sync();
       }
+      if (ok) ok = wait_warp(bar(L::kPFull + b), (t >> 1) & 1, kSiteKvMmaP | (b << 7) | (t & 0x7f));
+      if (!ok) break;
+      tc_fence_after_sync();
       if (leader) {
         issue_g(t);
         if ((t & 3) == 3) mma_commit(bar(L::kEmpty + (t >> 2) % L::kStages));  // Q_i, dO_i done
