@@ -590,7 +590,8 @@ def run_ours(args, world, rank, local):
         "shard": {"rank": rank, "world": world, "first": first, "count": count, "units": units},
         "pct_of_peak": 100.0 * achieved / peak,
         "ms_per_launch": {"mean": ms_max / args.steps, "median": statistics.median(per_launch),
-                          "min": min(per_launch), "max": max(per_launch)},
+                          "min": min(per_launch), "max": max(per_launch),
+                          "all": [round(x, 4) for x in per_launch]},
         "executed_over_counted_flops": executed_flops(w.B, w.H, w.S, w.D, w.causal) / flops,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
