@@ -308,6 +308,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq256_kernel(const __
     }
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
+    // The whole warp runs the issue code; each product and commit is
+    // predicated on the elected lane (mma_ts_p and co.), so that the warp
+    // never branches around them: the waits stay warp-wide and converged,
+    // which measured faster than a branch around each step's products.
     const bool leader = elect_one();
     constexpr uint32_t kIdescS = instr_desc_16bit(kRowsW, kStepW, false, false, F16);
     constexpr uint32_t kIdescQ = instr_desc_16bit(kRowsW, 256, false, true, F16);
@@ -328,33 +332,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq256_kernel(const __
                              kSiteW2MmaKV | 0x80 | (s & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader && dbg_smem(dbb, sb + L::kKOff + ks * kTile64, kTile64, 1024, kChkWMmaA) &&
+      if (dbg_smem(dbb, sb + L::kKOff + ks * kTile64, kTile64, 1024, kChkWMmaA) &&
           dbg_smem(dbb, sb + L::kVOff + vs * kTile64, kTile64, 1024, kChkWMmaB)) {
         // S = Q · K_sᵀ (A = Q from TMEM) and dP = dO · V_sᵀ (both from shared memory)
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
-          mma_ts(tmem_base + L::kSCol, tmem_base + L::kQCol + kk * 8,
-                 d_k + ks * kTileUnits + kstep_off(kk, kBlk64), kIdescS, kk > 0 ? 1u : 0u);
+          mma_ts_p(leader, tmem_base + L::kSCol, tmem_base + L::kQCol + kk * 8,
+                   d_k + ks * kTileUnits + kstep_off(kk, kBlk64), kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
-          mma_ss(tmem_base + L::kPCol, d_do + kstep_off(kk, kBlk128),
-                 d_v + vs * kTileUnits + kstep_off(kk, kBlk64), kIdescS, kk > 0 ? 1u : 0u);
-        mma_commit(bar(L::kSFull));
-        mma_commit(bar(L::kVEmpty + vs));
+          mma_ss_p(leader, tmem_base + L::kPCol, d_do + kstep_off(kk, kBlk128),
+                   d_v + vs * kTileUnits + kstep_off(kk, kBlk64), kIdescS, kk > 0 ? 1u : 0u);
+        mma_commit_p(leader, bar(L::kSFull));
+        mma_commit_p(leader, bar(L::kVEmpty + vs));
       }
-      __syncwarp();
       ok = wait_warp(bar(L::kPFull), s & 1, kSiteW2MmaP | (s & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader) {
-        // dQ += dS · K_s (16 keys per step; K_s as an MN-major operand)
+      // dQ += dS · K_s (16 keys per step; K_s as an MN-major operand)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem_base + L::kDqCol, tmem_base + L::kSCol + split_col(kk),
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ts_p(leader, tmem_base + L::kDqCol, tmem_base + L::kSCol + split_col(kk),
                  d_kmn + ks * kTileUnits + kk * (2048 >> 4), kIdescQ, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(L::kKEmpty + ks));  // the next S overwrites dS: issued after these
-      }
-      __syncwarp();
+      mma_commit_p(leader, bar(L::kKEmpty + ks));  // the next S overwrites dS: issued after these
     }
     if (leader) {
       if (ok) mma_commit(bar(L::kOFull));
@@ -648,6 +648,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_q64_kernel(const
     __syncwarp();
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
+    // The whole warp runs the issue code; each product and commit is
+    // predicated on the elected lane (mma_ts_p and co.), so that the warp
+    // never branches around them: the waits stay warp-wide and converged,
+    // which measured faster than a branch around each step's products.
     const bool leader = elect_one();
     constexpr uint32_t kIdescS = instr_desc_16bit(kRowsW, kStepW, false, false, F16);
     constexpr uint32_t kIdescG = instr_desc_16bit(kRowsW, kCols, false, true, F16);
@@ -670,40 +674,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_q64_kernel(const
       ok = wait_warp(bar(L::kFull + st), (t / L::kStages) & 1, kSiteW3MmaQ | (t & 0xff));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader && dbg_smem(dbb, sb + L::kQOff + st * kTileQ, kTileQ, 1024, kChkWMmaA) &&
+      if (dbg_smem(dbb, sb + L::kQOff + st * kTileQ, kTileQ, 1024, kChkWMmaA) &&
           dbg_smem(dbb, sb + L::kDoOff + st * kTileQ, kTileQ, 1024, kChkWMmaB)) {
         // Sᵀ = K · Q_tᵀ (A = K from TMEM) and dPᵀ = V · dO_tᵀ (A = V from
         // TMEM, or from shared memory when the head dimension is split)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem_base + L::kSCol, tmem_base + L::kKCol + kk * 8,
-                 d_q + st * kTileUnits + kstep_off(kk, kBlk64), kIdescS, kk > 0 ? 1u : 0u);
+          mma_ts_p(leader, tmem_base + L::kSCol, tmem_base + L::kKCol + kk * 8,
+                   d_q + st * kTileUnits + kstep_off(kk, kBlk64), kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t db = d_do + st * kTileUnits + kstep_off(kk, kBlk64);
           if constexpr (kSplit)
-            mma_ss(tmem_base + L::kPCol, d_v + kstep_off(kk, kBlk128), db, kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss_p(leader, tmem_base + L::kPCol, d_v + kstep_off(kk, kBlk128), db, kIdescS,
+                     kk > 0 ? 1u : 0u);
           else
-            mma_ts(tmem_base + L::kPCol, tmem_base + L::kVCol + kk * 8, db, kIdescS, kk > 0 ? 1u : 0u);
+            mma_ts_p(leader, tmem_base + L::kPCol, tmem_base + L::kVCol + kk * 8, db, kIdescS,
+                     kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::kSFull));
+        mma_commit_p(leader, bar(L::kSFull));
       }
-      __syncwarp();
       ok = wait_warp(bar(L::kPFull), t & 1, kSiteW3MmaP | (t & 0xff));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader) {
-        // dV += Pᵀ · dO_t and dK += dSᵀ · Q_t over this CTA's columns (16 queries per step)
+      // dV += Pᵀ · dO_t and dK += dSᵀ · Q_t over this CTA's columns (16 queries per step)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t bo = st * kTileUnits + kk * (2048 >> 4);
-          mma_ts(tmem_base + L::kDvCol, tmem_base + L::kSCol + split_col(kk), d_do_mn + bo, kIdescG, acc);
-          mma_ts(tmem_base + L::kDkCol, tmem_base + L::kPCol + split_col(kk), d_q_mn + bo, kIdescG, acc);
-        }
-        mma_commit(bar(L::kEmpty + st));  // the next Sᵀ, dPᵀ overwrite Pᵀ, dSᵀ: issued after these
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+        const uint32_t bo = st * kTileUnits + kk * (2048 >> 4);
+        mma_ts_p(leader, tmem_base + L::kDvCol, tmem_base + L::kSCol + split_col(kk), d_do_mn + bo,
+                 kIdescG, acc);
+        mma_ts_p(leader, tmem_base + L::kDkCol, tmem_base + L::kPCol + split_col(kk), d_q_mn + bo,
+                 kIdescG, acc);
       }
-      __syncwarp();
+      mma_commit_p(leader, bar(L::kEmpty + st));  // the next Sᵀ, dPᵀ overwrite Pᵀ, dSᵀ: issued after these
     }
     if (leader) {
       if (ok) mma_commit(bar(L::kOFull));

@@ -330,6 +330,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     }
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
+    // The whole warp runs the issue code; each product and commit is
+    // predicated on the elected lane (mma_ts_p and co.), so that the warp
+    // never branches around them: the waits stay warp-wide and converged,
+    // which measured faster than a branch around each step's products.
     const bool leader = elect_one();
     constexpr uint32_t kIdescSP = instr_desc_16bit(kTileRows, 64, false, false, F16);  // 64 keys
     constexpr uint32_t kIdescQ = instr_desc_16bit(kTileRows, D, false, true, F16);
@@ -350,22 +354,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ts(tmem_base + 128 * h, tmem_base + L::kQCol + kk * 8,
+        mma_ts_p(leader, tmem_base + 128 * h, tmem_base + L::kQCol + kk * 8,
                dk + ks * kTileUnits + h * kHalfUnits + off, kIdescSP, kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ts(tmem_base + 128 * h + 64, tmem_base + L::kDoCol + kk * 8,
+        mma_ts_p(leader, tmem_base + 128 * h + 64, tmem_base + L::kDoCol + kk * 8,
                dv + vs * kTileUnits + h * kHalfUnits + off, kIdescSP, kk > 0 ? 1u : 0u);
       }
-      mma_commit(bar(L::kSFull + h));
+      mma_commit_p(leader, bar(L::kSFull + h));
     };
     // G(j, h): dQ += dS_h · K_j[64h, 64h+64) (16 key rows per step)
     auto issue_g = [&](int ks, int h, bool first) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_ts(tmem_base + 256, tmem_base + 128 * h + kk * 8,
+        mma_ts_p(leader, tmem_base + 256, tmem_base + 128 * h + kk * 8,
                dk_mn + ks * kTileUnits + (4 * h + kk) * (2048 >> 4), kIdescQ,
                (first && kk == 0) ? 0u : 1u);
     };
@@ -381,12 +385,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     if (ok) ok = wait_kv(0);
     if (ok) {
       tc_fence_after_sync();
-      if (leader) {
-        issue_sp(0, 0, 0);
-        issue_sp(0, 0, 1);
-        mma_commit(bar(L::kVEmpty + 0));
-      }
-      __syncwarp();
+      issue_sp(0, 0, 0);
+      issue_sp(0, 0, 1);
+      mma_commit_p(leader, bar(L::kVEmpty + 0));
     }
     for (int j = 0; j < nkv && ok; ++j) {
       const int ks = j % L::kKStages;
@@ -401,29 +402,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       if (ok) ok = wait_warp(bar(L::kPFull + 0), j & 1, kSiteDqMmaP | (j & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader) issue_g(ks, 0, j == 0);
-      __syncwarp();
+      issue_g(ks, 0, j == 0);
       if (more) {
         if (!kKvFirst) {
           ok = wait_kv(j + 1);
           if (!ok) break;
           tc_fence_after_sync();
         }
-        if (leader) issue_sp(ksn, vsn, 0);
-        __syncwarp();
+        issue_sp(ksn, vsn, 0);
       }
       ok = wait_warp(bar(L::kPFull + 1), j & 1, kSiteDqMmaP | 0x80 | (j & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader) {
-        issue_g(ks, 1, false);
-        mma_commit(bar(L::kKEmpty + ks));  // K_j: last read by G(j, 1)
-        if (more) {
-          issue_sp(ksn, vsn, 1);
-          mma_commit(bar(L::kVEmpty + vsn));  // V_{j+1}: last read by SP(j+1, 1)
-        }
+      issue_g(ks, 1, false);
+      mma_commit_p(leader, bar(L::kKEmpty + ks));  // K_j: last read by G(j, 1)
+      if (more) {
+        issue_sp(ksn, vsn, 1);
+        mma_commit_p(leader, bar(L::kVEmpty + vsn));  // V_{j+1}: last read by SP(j+1, 1)
       }
-      __syncwarp();
     }
     if (leader) {
       if (ok) mma_commit(bar(L::kOFull));
@@ -706,6 +702,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
     __syncwarp();
   } else {
     // ======================= tcgen05 issuer (warp 8) =======================
+    // The whole warp runs the issue code; each product and commit is
+    // predicated on the elected lane (mma_ts_p and co.), so that the warp
+    // never branches around them: the waits stay warp-wide and converged,
+    // which measured faster than a branch around each step's products.
     const bool leader = elect_one();
     constexpr uint32_t kIdescSP = instr_desc_16bit(kTileRows, 32, false, false, F16);  // 32 queries
     constexpr uint32_t kIdescG = instr_desc_16bit(kTileRows, D, false, true, F16);
@@ -729,16 +729,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ts(tmem_base + 64 * b, tmem_base + L::kKCol + kk * 8, dq + bq + off, kIdescSP,
+        mma_ts_p(leader, tmem_base + 64 * b, tmem_base + L::kKCol + kk * 8, dq + bq + off, kIdescSP,
                kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ts(tmem_base + 64 * b + 32, tmem_base + L::kVCol + kk * 8, ddo + bq + off, kIdescSP,
+        mma_ts_p(leader, tmem_base + 64 * b + 32, tmem_base + L::kVCol + kk * 8, ddo + bq + off, kIdescSP,
                kk > 0 ? 1u : 0u);
       }
-      mma_commit(bar(L::kSFull + b));
+      mma_commit_p(leader, bar(L::kSFull + b));
     };
     // G(t): dV += Pᵀ · dO_i[32q, 32q+32), dK += dSᵀ · Q_i[32q, 32q+32)
     auto issue_g = [&](int t) {
@@ -748,8 +748,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
         const uint32_t a = 64 * b + kk * 8;
         const uint32_t bo = st * kTileUnits + (2 * q + kk) * (2048 >> 4);
         const uint32_t acc = (t == 0 && kk == 0) ? 0u : 1u;
-        mma_ts(tmem_base + L::kDvCol, tmem_base + a, ddo_mn + bo, kIdescG, acc);
-        mma_ts(tmem_base + L::kDkCol, tmem_base + a + 32, dq_mn + bo, kIdescG, acc);
+        mma_ts_p(leader, tmem_base + L::kDvCol, tmem_base + a, ddo_mn + bo, kIdescG, acc);
+        mma_ts_p(leader, tmem_base + L::kDkCol, tmem_base + a + 32, dq_mn + bo, kIdescG, acc);
       }
     };
 
@@ -757,11 +757,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
     if (ok) ok = wait_warp(bar(L::kFull + 0), 0, kSiteKvMmaQ);
     if (ok) {
       tc_fence_after_sync();
-      if (leader) {
-        issue_sp(0);
-        issue_sp(1);
-      }
-      __syncwarp();
+      issue_sp(0);
+      issue_sp(1);
     }
     for (int t = 0; t < n_sub && ok; ++t) {
       const int b = t & 1;
@@ -776,12 +773,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       if (ok) ok = wait_warp(bar(L::kPFull + b), (t >> 1) & 1, kSiteKvMmaP | (b << 7) | (t & 0x7f));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader) {
-        issue_g(t);
-        if ((t & 3) == 3) mma_commit(bar(L::kEmpty + (t >> 2) % L::kStages));  // Q_i, dO_i done
-        if (t2 < n_sub) issue_sp(t2);
-      }
-      __syncwarp();
+      issue_g(t);
+      if ((t & 3) == 3) mma_commit_p(leader, bar(L::kEmpty + (t >> 2) % L::kStages));  // Q_i, dO_i done
+      if (t2 < n_sub) issue_sp(t2);
     }
     if (leader) {
       if (ok) mma_commit(bar(L::kOFull));

@@ -377,6 +377,10 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
     }
   } else {
     // ======================= tcgen05 issuer (warp 4) =======================
+    // The whole warp runs the issue code; each product and commit is
+    // predicated on the elected lane (mma_ts_p and co.), so that the warp
+    // never branches around them: the waits stay warp-wide and converged,
+    // which measured faster than a branch around each step's products.
     const bool leader = elect_one();
     constexpr uint32_t kIdescS = instr_desc_16bit(kQRows, kKvRows, false, false, F16);
     constexpr uint32_t kIdescO = instr_desc_16bit(kQRows, kD, false, true, F16);
@@ -396,19 +400,18 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ts(tmem_base + BN * (j & 1), tmem_base + kQCol + kk * 8, db + off, kIdescS,
-               kk > 0 ? 1u : 0u);
+        mma_ts_p(leader, tmem_base + BN * (j & 1), tmem_base + kQCol + kk * 8, db + off, kIdescS,
+                 kk > 0 ? 1u : 0u);
       }
-      mma_commit(bar(kSFull + (j & 1)));
-      mma_commit(bar(kKEmpty + j % kKStages));
+      mma_commit_p(leader, bar(kSFull + (j & 1)));
+      mma_commit_p(leader, bar(kKEmpty + j % kKStages));
     };
     bool ok = wait_warp(bar(kQTmem), 0, kSiteMmaQ);
     for (int j0 = 0; j0 < 2 && j0 < nkv && ok; ++j0) {
       ok = wait_warp(bar(kKFull + j0 % kKStages), (j0 / kKStages) & 1, kSiteMmaK | j0);
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader) issue_s(j0);
-      __syncwarp();
+      issue_s(j0);
     }
     for (int j = 0; j < nkv && ok; ++j) {
       const int b = j & 1;
@@ -416,24 +419,22 @@ __global__ void __launch_bounds__(kThreads1Q, 1) attn_fwd_1q_kernel(const __grid
       if (ok) ok = wait_warp(bar(kVFull + j % kVStages), (j / kVStages) & 1, kSiteMmaV | (j & 0xff));
       if (!ok) break;
       tc_fence_after_sync();
-      if (leader && dbg_smem(dbb, sb + kVOff + (j % kVStages) * kTile, kTile, 1024, kChkMmaV) &&
+      if (dbg_smem(dbb, sb + kVOff + (j % kVStages) * kTile, kTile, 1024, kChkMmaV) &&
           dbg_tmem_cols(dbb, tmem_base + kOCol, kD, kChkMmaTmem)) {
         const uint64_t db = dv + (j % kVStages) * kTileUnits;
 #pragma unroll
         for (int kk = 0; kk < kKvRows / 16; ++kk)  // O += P_b · V_j, 16 keys per step
-          mma_ts(tmem_base + kOCol, tmem_base + BN * b + kk * 8, db + kk * (2048 >> 4), kIdescO,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(kPvDone));
-        mma_commit(bar(kVEmpty + j % kVStages));
+          mma_ts_p(leader, tmem_base + kOCol, tmem_base + BN * b + kk * 8, db + kk * (2048 >> 4),
+                   kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_p(leader, bar(kPvDone));
+        mma_commit_p(leader, bar(kVEmpty + j % kVStages));
       }
-      __syncwarp();
       if (j + 2 < nkv) {
         ok = wait_warp(bar(kKFull + (j + 2) % kKStages), ((j + 2) / kKStages) & 1,
                        kSiteMmaK | ((j + 2) & 0xff));
         if (!ok) break;
         tc_fence_after_sync();
-        if (leader) issue_s(j + 2);  // overwrites P_b: PV_j was issued first
-        __syncwarp();
+        issue_s(j + 2);  // overwrites P_b: PV_j was issued first
       }
     }
     if (leader) {
