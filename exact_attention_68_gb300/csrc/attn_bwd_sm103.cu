@@ -243,15 +243,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
       for (int e2 = 0; e2 < 32; ++e2) {
         const int h = e2 >> 4;
         const int e = (2 * e2) & 31;
-        float p0 = ex2_approx(fmaf(__uint_as_float(s[h][e]), sl2, -lse2));
-        float p1 = ex2_approx(fmaf(__uint_as_float(s[h][e + 1]), sl2, -lse2));
+        // key pairs in packed f32x2 arithmetic (the same roundings as the
+        // scalar form, half the FP32 instructions)
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[h][e]), __uint_as_float(s[h][e + 1])),
+                                    make_float2(sl2, sl2), make_float2(-lse2, -lse2));
+        float p0 = ex2_approx(x.x);
+        float p1 = ex2_approx(x.y);
         if (edge) {
           if (2 * e2 > lim) p0 = 0.f;
           if (2 * e2 + 1 > lim) p1 = 0.f;
         }
-        const float ds0 = p0 * (__uint_as_float(dp[h][e]) - delta);
-        const float ds1 = p1 * (__uint_as_float(dp[h][e + 1]) - delta);
-        pk[e2] = pack_x2<F16>(ds0, ds1);
+        const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[h][e]), __uint_as_float(dp[h][e + 1])),
+                                     make_float2(-delta, -delta));
+        const float2 ds = __fmul2_rn(make_float2(p0, p1), dd);
+        pk[e2] = pack_x2<F16>(ds.x, ds.y);
       }
       tmem_st_32x32b_x32(tS, pk);
       tmem_st_wait();
@@ -452,7 +457,7 @@ struct KvLayout {
   static constexpr int kTile = kTileRows * D * 2;
   static constexpr int kChunks = D / 64;
   static constexpr int kStages = (D == 128) ? 3 : 4;  // Q/dO ring depth
-  static constexpr int kStatBytes = 2 * kTileRows * 4;  // (lse·log2e, delta) per query row
+  static constexpr int kStatBytes = 2 * kTileRows * 4;  // (−lse·log2e, −delta) per query row
   static constexpr int kQOff = 0;
   static constexpr int kDoOff = kQOff + kStages * kTile;
   static constexpr int kStatOff = kDoOff + kStages * kTile;
@@ -595,22 +600,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
       int lo = CAUSAL ? gk - c0 : 0;
       if (gk >= p.S) lo = 32;  // key row past the end: nothing
       const bool edge = lo > 0 || hi < 31;
-      // (lse·log2e, delta) of this quarter's 32 query columns, two columns per load
+      // (−lse·log2e, −delta) of this quarter's 32 query columns, two columns per load
       const float4* stat = reinterpret_cast<const float4*>(
           smem_gen + L::kStatOff + st * L::kStatBytes + 8 * 32 * q);
       uint32_t ppk[16], dpk[16];
 #pragma unroll
       for (int e2 = 0; e2 < 16; ++e2) {
         const int c = 2 * e2;
-        const float4 sd = stat[e2];  // lse2[c], delta[c], lse2[c+1], delta[c+1]
-        float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -sd.x));
-        float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, -sd.z));
+        const float4 sd = stat[e2];  // -lse2[c], -delta[c], -lse2[c+1], -delta[c+1]
+        // column pairs in packed f32x2 arithmetic at D = 128 (the same roundings
+        // as the scalar form; measured faster there, slower at D = 64)
+        constexpr bool kPacked = D == 128;
+        float p0, p1;
+        if constexpr (kPacked) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])),
+                                      make_float2(sl2, sl2), make_float2(sd.x, sd.z));
+          p0 = ex2_approx(x.x);
+          p1 = ex2_approx(x.y);
+        } else {
+          p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, sd.x));
+          p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, sd.z));
+        }
         if (edge) {
           if (c < lo || c > hi) p0 = 0.f;
           if (c + 1 < lo || c + 1 > hi) p1 = 0.f;
         }
-        const float ds0 = p0 * (__uint_as_float(dp[c]) - sd.y);
-        const float ds1 = p1 * (__uint_as_float(dp[c + 1]) - sd.w);
+        float ds0, ds1;
+        if constexpr (kPacked) {
+          const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                       make_float2(sd.y, sd.w));
+          const float2 ds = __fmul2_rn(make_float2(p0, p1), dd);
+          ds0 = ds.x, ds1 = ds.y;
+        } else {
+          ds0 = p0 * (__uint_as_float(dp[c]) + sd.y);
+          ds1 = p1 * (__uint_as_float(dp[c + 1]) + sd.w);
+        }
         ppk[e2] = pack_x2<F16>(p0, p1);
         dpk[e2] = pack_x2<F16>(ds0, ds1);
       }
@@ -667,8 +691,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkdv_kernel(const __g
         const int c = lane + 32 * t;
         const int q = i * kTileRows + c;
         const bool in = q < p.S && dbg_row(dbb, bh, q, 0, 0, kChkStat);
-        st_shared_f32x2(stat + 8 * c, in ? p.lse[row0 + q] * kLog2e : 0.f,
-                        in ? p.delta[row0 + q] : 0.f);
+        st_shared_f32x2(stat + 8 * c, in ? -(p.lse[row0 + q] * kLog2e) : 0.f,
+                        in ? -p.delta[row0 + q] : 0.f);
       }
       __syncwarp();
       if (lane == 0) {
