@@ -23,23 +23,34 @@
 //                         dV += Pᵀ·dO, dK += dSᵀ·Q.
 //
 // GB300 mapping (per CTA): warps 0-7 do the elementwise work, one thread per
-// TMEM lane (a tile row); warp 8 issues tcgen05.mma (operands from shared
-// memory via TMA, 128-byte swizzle; the P / dS operands straight from TMEM);
-// warp 9 feeds the shared-memory rings with TMA.  Every 128-column tile of the
-// loop is handled as two 64-column halves with a TMEM buffer each, and
-// warpgroup g (warps 4g..4g+3) always takes half g: while one warpgroup does
-// its half's elementwise work, the tensor core runs the other half's MMAs.
-// The MMA order per step t is G(t,0), SP(t+1,0), G(t,1), SP(t+1,1), where SP
-// is a half's S/dP products and G its gradient products, so each half's
-// elementwise work is covered by about 1300 cycles of tensor work.
-// TMEM columns:
-//   dq kernel:    half h: S_h [128h, 128h+64), dP_h [128h+64, 128h+128);
-//                 dQ [256, 256+D)
-//   dk/dv kernel: half h: Sᵀ_h [128h, 128h+64), dPᵀ_h [128h+64, 128h+128);
-//                 dV [256, 256+D), dK [256+D, 256+2D)
-// A warpgroup stores its bf16 results (two per 32-bit column) over the first
-// 32 columns of the S and dP blocks it has just read: they are the A operand
-// of the half's gradient MMAs.
+// TMEM lane (a tile row), in two warpgroups with a TMEM buffer each; warp 8
+// issues tcgen05.mma (the whole warp runs the issue code, each product and
+// commit predicated on its elected lane); warp 9 feeds the shared-memory
+// rings with TMA.  While one warpgroup does its buffer's elementwise work,
+// the tensor core runs the other buffer's products.
+//
+//   dq kernel     Q and dO rows are put into TMEM once (the A operand of every
+//                 S and dP product); K/V tiles stream through shared memory.
+//                 Each K/V tile is two 64-key halves, warpgroup g always
+//                 taking half g; the MMA order per tile j is G(j,0),
+//                 SP(j+1,0), G(j,1), SP(j+1,1) (SP: a half's S and dP
+//                 products, G: its dQ product).  TMEM: half h's S [128h,
+//                 128h+64) and dP [128h+64, 128h+128); dQ [256, 256+D);
+//                 Q [384, 384+D/2), dO [384+D/2, 384+D).
+//   dk/dv kernel  K and V rows are put into TMEM once (the A operand of every
+//                 Sᵀ and dPᵀ product); Q and dO tiles stream through shared
+//                 memory.  Each Q tile is four 32-query sub-steps, warpgroup b
+//                 taking the sub-steps t ≡ b (mod 2); the MMA order is G(t),
+//                 then SP(t+2) into the buffer G(t) has just read.  TMEM:
+//                 buffer b's Sᵀ [64b, 64b+32) and dPᵀ [64b+32, 64b+64);
+//                 K [128, 128+D/2), V [128+D/2, 128+D); dV [256, 256+D),
+//                 dK [256+D, 256+2D).
+//
+// A warpgroup stores its 16-bit results (two per 32-bit column) over the
+// first columns of the S and dP blocks it has just read: they are the A
+// operand of the gradient products.  The elementwise arithmetic runs on
+// packed f32x2 pairs (in the dk/dv kernel at D = 128 only), with the same
+// roundings as the scalar form.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
