@@ -402,7 +402,8 @@ def side_workloads(device, stream, kept=None):
     res[WORKLOAD + "_fp16"] = {"about": w.about + ", fp16 inputs", "ms": ms,
                                "tflops": counted_flops(w.B, w.H, w.S, w.D, w.causal) / (ms * 1e-3) / 1e12}
     # other head dimensions at the long-context shape (the same 16384-key rows):
-    # 256 has its own kernel width, 96 and 192 run on the next width up
+    # 256 and 192 have their own forward kernel widths, 96 runs on the next
+    # width up
     for D, H in ((256, 16), (96, 32), (192, 16)):
         gen = torch.Generator(device=device).manual_seed(D)
         q, k, v = (torch.randn((1, H, 16384, D), generator=gen, device=device).to(torch.bfloat16)

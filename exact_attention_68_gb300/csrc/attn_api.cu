@@ -160,16 +160,16 @@ attn_status_t launch_with_status(const void* q, const void* k, const void* v, vo
                                  float scale, int causal, bool f16, uint64_t timeout_ns,
                                  int* status, cudaStream_t stream) {
   const int64_t BH = B * H;
-  // The kernels exist for 64, 128 and 256 columns; another head dimension
-  // runs on the next one up.  The tensor maps carry the real column count,
+  // The kernels exist for 64, 128, 192 and 256 columns; another head
+  // dimension runs on the next one up.  The tensor maps carry the real column count,
   // so TMA loads read zeros past it and stores leave those columns out; the
   // zero columns add nothing to q·kᵀ and give zero output columns.
-  const int dk = kernel_head_dim(D);
+  const int dk = forward_head_dim(D);
   // 64 and 128 columns: the persistent kernel (one CTA per SM walking Q
-  // tiles); 256 columns: one Q tile per CTA with 64-row K/V tiles (its output
-  // tile does not fit the persistent kernel's staging buffer).
+  // tiles); 192 and 256 columns: one Q tile per CTA with 64-row K/V tiles
+  // (their output tile does not fit the persistent kernel's staging buffer).
   const bool persistent = dk <= 128;
-  const int bn = dk == 256 ? 64 : 128;  // rows of one K/V tile
+  const int bn = dk > 128 ? 64 : 128;  // rows of one K/V tile
   Fwd1QParams p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_bhsd_16bit(&p.tm_k, k, BH, S, D, bn, f16) ||

@@ -1,6 +1,6 @@
 // attn_fwd_1q_sm103.cu — the fused attention forward with one Q tile per CTA
-// on GB300 (sm_103a), for head dimension 256 (the persistent kernel runs the
-// narrower ones).
+// on GB300 (sm_103a), for head dimensions 192 and 256 (the persistent kernel
+// runs the narrower ones).
 //
 // Same computation as the D = 64 / 128 kernel: out = softmax(scale·q·kᵀ +
 // causal mask)·v per (batch, head) with the row logsumexp, following the five
@@ -9,8 +9,8 @@
 // [S, S] scores never leave the chip (same page, "Why flash attention exists";
 // FlashAttention-2 blog, "FlashAttention-2 Optimizations" §1-§3).
 //
-// Layout: one 128-row Q tile per CTA, K/V tiles of BN rows (64 at D = 256,
-// 128 at D = 128), and two BN-column S buffers, so that the next S is computed
+// Layout: one 128-row Q tile per CTA, K/V tiles of BN rows (64 at D = 192
+// and 256), and two BN-column S buffers, so that the next S is computed
 // while the softmax of the current one runs: the softmaxes of one tile follow
 // each other back to back.  Q is the A operand of every S product of the CTA:
 // it is put into TMEM once, so S = Q·Kᵀ is a TS product and shared memory only
@@ -47,8 +47,10 @@ template <int D, int BN>
 struct Layout1Q {
   static constexpr int kChunkBytes = BN * 128;   // one 64-column block of a K/V tile
   static constexpr int kTile = BN * D * 2;       // one K/V tile
-  static constexpr int kKStages = (kTile >= 32768) ? 3 : 5;
-  static constexpr int kVStages = (kTile >= 32768) ? 3 : 5;
+  // ring stages: as many as shared memory holds, up to 5 (32 KB tiles: 3,
+  // 24 KB: 4)
+  static constexpr int kKStages = (kTile >= 32768) ? 3 : (kTile > 16384) ? 4 : 5;
+  static constexpr int kVStages = kKStages;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKStages * kTile;
   static constexpr int kBarOff = kVOff + kVStages * kTile;
@@ -468,10 +470,16 @@ cudaError_t launch_1q(const Fwd1QParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+template <int D>
+cudaError_t launch_1q_d(const Fwd1QParams& p, bool causal, bool f16, cudaStream_t stream) {
+  if (f16) return causal ? launch_1q<D, 64, true, true>(p, stream) : launch_1q<D, 64, false, true>(p, stream);
+  return causal ? launch_1q<D, 64, true, false>(p, stream) : launch_1q<D, 64, false, false>(p, stream);
+}
+
 cudaError_t fwd1q_launch(const Fwd1QParams& p, int D, bool causal, bool f16, cudaStream_t stream) {
-  if (D != 256) return cudaErrorInvalidValue;
-  if (f16) return causal ? launch_1q<256, 64, true, true>(p, stream) : launch_1q<256, 64, false, true>(p, stream);
-  return causal ? launch_1q<256, 64, true, false>(p, stream) : launch_1q<256, 64, false, false>(p, stream);
+  if (D == 192) return launch_1q_d<192>(p, causal, f16, stream);
+  if (D == 256) return launch_1q_d<256>(p, causal, f16, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ea

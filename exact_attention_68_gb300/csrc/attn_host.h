@@ -45,6 +45,9 @@ inline cudaError_t current_device_bound(int* dev) {
 // Columns of the kernel that runs a head dimension D (a multiple of 8, at
 // most 256): the smallest of 64, 128, 256 that holds D.
 inline int kernel_head_dim(int64_t D) { return D <= 64 ? 64 : D <= 128 ? 128 : 256; }
+// The forward also has a kernel 192 columns wide, so that head dimensions
+// 136-192 do not pay for 256.
+inline int forward_head_dim(int64_t D) { return D <= 128 ? kernel_head_dim(D) : D <= 192 ? 192 : 256; }
 
 // The status a non-zero device status word reports: its bits are 1 (a wait
 // ran out) and 2 (an index check of a debug build failed).

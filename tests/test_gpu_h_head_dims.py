@@ -1,6 +1,7 @@
 """GPU parity of head dimensions other than 64, 128 and 256 against the fp64
 oracle.  They run on the kernel of the next width up (64, 128 or 256
-columns) with the columns past D read as zero by TMA and never stored; the
+columns; the forward also has 192) with the columns past D read as zero by
+TMA and never stored; the
 tests check the results against the oracle with the same bars as the native
 widths, and that nothing past the end of each output tensor is written."""
 import numpy as np

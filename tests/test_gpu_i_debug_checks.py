@@ -44,7 +44,7 @@ def _fwd(lib, q, k, v, scale, causal):
 
 FWD_CASES = [(64, (1, 2, 1)), (64, (2, 1, 300)), (128, (1, 2, 129)), (128, (2, 2, 1000)),
              (256, (1, 2, 65)), (256, (1, 1, 513)), (32, (1, 2, 200)), (96, (2, 1, 257)),
-             (192, (1, 2, 130)), (8, (1, 1, 77)),
+             (192, (1, 2, 130)), (136, (2, 1, 200)), (8, (1, 1, 77)),
              # long enough that the persistent kernel takes the path whose
              # softmax warps load Q (more than 24 K/V steps a tile on average
              # under both masks), ragged in S
