@@ -407,7 +407,7 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// As mma_ts and mma_commit, executed by the whole (converged) warp: only the
+// As mma_ts, mma_ss and mma_commit, executed by the whole (converged) warp: only the
 // lane whose `issue` is true issues, so the warp never branches around them.
 __device__ __forceinline__ void mma_ts_p(bool issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {

@@ -19,12 +19,16 @@ pytestmark = pytest.mark.gpu
 def unit_lib(cuda_device):
     lib = ctypes.CDLL(build_unit_library())
     lib.umma_unit_run.restype = ctypes.c_int
-    lib.umma_unit_run.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int]
+    lib.umma_unit_run.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_int, ctypes.c_int]
     return lib
 
 
+@pytest.mark.parametrize("predicated", [0, 1], ids=["lane0", "predicated"])
 @pytest.mark.parametrize("D", [64, 128])
-def test_qk_and_pv_mma_are_exact(unit_lib, D):
+def test_qk_and_pv_mma_are_exact(unit_lib, D, predicated):
+    # predicated: the whole MMA warp runs the issue path with each product and
+    # commit predicated on lane 0 (the backward kernels' form); a product
+    # issued by more than one lane would accumulate more than once
     g = torch.Generator().manual_seed(D)
     a = torch.randint(-2, 3, (128, D), generator=g).to(torch.bfloat16)
     b = torch.randint(-2, 3, (128, D), generator=g).to(torch.bfloat16)
@@ -40,7 +44,7 @@ def test_qk_and_pv_mma_are_exact(unit_lib, D):
     o_out = torch.full((128, D), float("nan"), device=dev)
     status = torch.zeros(2, dtype=torch.int32, device=dev)
     rc = unit_lib.umma_unit_run(ad.data_ptr(), bd.data_ptr(), vd.data_ptr(), pd.data_ptr(),
-                                s_out.data_ptr(), o_out.data_ptr(), status.data_ptr(), D)
+                                s_out.data_ptr(), o_out.data_ptr(), status.data_ptr(), D, predicated)
     assert rc == 0
     assert status.cpu().tolist() == [0, 0]
     s_ref = a.double().numpy() @ b.double().numpy().T
